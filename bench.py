@@ -1,0 +1,368 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused FP4 paged-MQA indexer prefill + exact TopK on GB300.
+
+Workload (default): Q=8192 rows, H=64, D=128, K=1024, C4 context 196,608 (the
+V4-Pro-shaped prefill of "[FlyDSL] Add FP4 LiteTopK prefill operator",
+ROCm/aiter#5309, Validation table), one request whose rows are its last 8192
+raw tokens, causal windows, shuffled page table, seeded synthetic FP4/UE8M0
+values.
+
+One step = one idx_topk_fp4_prefill call (plan, page validation, fused
+score+select, merge+map, status read-back) on inputs resident in HBM; L2 is
+flushed (256 MiB write) before every timed step, outside the step's events.
+Metric value = algorithmic FP4 FLOP (2*64*128 per scored (row, slot)) per
+second, summed over ranks (each rank runs the whole workload: weak scaling).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused score+TopK ms & FP4 TFLOPS (% peak) at Q=8192, C4=196608, K=1024"
+NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense FP4 : bf16 tensor ratio of GB300
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--config", type=int, default=3, help="workload index (default 3)")
+    ap.add_argument("--pairs", type=int, default=15, help="alternating dense/fused pairs")
+    ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def score_kernel_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp4_sparse_attention_tma_gb300", "csrc")
+    for name in ("score.cu", "idx_device.cuh", "idx_select.cuh", "idx_internal.h"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch of the scoring kernel from the committed ncu
+    summary, only when it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "score_kernel_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("kernel_sha") == score_kernel_sha() and d.get("workload") == workload:
+            return d.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                n += 1
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+def cpu_baseline(p, seconds: float):
+    """The oracle, as it stands, on a bounded sample of rows of the workload."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    K = p.topk
+    scored = np.nonzero(p.lengths() > K)[0]
+    t0 = time.perf_counter()
+    oracle.prefill_rows(p, rows=scored[-1:].astype(np.int32))
+    t_row = max(time.perf_counter() - t0, 1e-3)
+    n = int(max(1, min(len(scored), seconds / t_row)))
+    pick = scored[np.linspace(0, len(scored) - 1, n).astype(np.int64)].astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.prefill_rows(p, rows=pick)
+    dt = time.perf_counter() - t0
+    flop = float(p.lengths()[pick].sum()) * 2 * 64 * 128
+    return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": f"{n} of {len(scored)} scored rows (evenly spaced), full windows, "
+                      f"{dt:.1f} s wall",
+            "seconds": dt}
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle on the host cores, same metric and workload."""
+    import numpy as np
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from fp4_sparse_attention_tma_gb300 import inputs
+    oracle.build()
+    p = inputs.config(args.config)
+    scored = np.nonzero(p.lengths() > p.topk)[0]
+    t0 = time.perf_counter()
+    oracle.prefill_rows(p, rows=scored[-1:].astype(np.int32))
+    t_row = max(time.perf_counter() - t0, 1e-3)
+    budget = 150.0
+    per_step = int(max(1, min(64, budget / (args.steps + args.warmup) / t_row)))
+    rng = np.random.default_rng(0)
+    times, flops = [], []
+    for i in range(args.warmup + args.steps):
+        pick = np.sort(rng.choice(scored, size=per_step, replace=False)).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.prefill_rows(p, rows=pick)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+            flops.append(float(p.lengths()[pick].sum()) * 2 * 64 * 128)
+    value = sum(flops) / sum(times) / 1e12
+    sample = f"{per_step} random scored rows per step (full windows) of the workload"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": p.name, "rows": p.rows, "c4_context": p.max_end(),
+                       "topk": p.topk},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import fp4_sparse_attention_tma_gb300 as m
+    from fp4_sparse_attention_tma_gb300 import inputs
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    p = inputs.config(args.config)
+    R, K = p.rows, p.topk
+    flop = float(p.algorithmic_flop())
+    host = dict(q_fp4=p.q_fp4, q_scale=p.q_scale, k_cache_fp4=p.k_cache_fp4, k_scale=p.k_scale,
+                weights=p.weights, page_table=p.page_table, row_req=p.row_req,
+                row_start=p.row_start, row_end=p.row_end)
+    dev = {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in host.items()}
+    phys = torch.empty((R, K), dtype=torch.int32, device="cuda")
+    raw = torch.empty((R, K), dtype=torch.int32, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def fused():
+        m.idx_topk_fp4_prefill(**dev, topk=K, out_phys_slot=phys, out_raw_idx=raw)
+
+    m.idx_topk_set_timing(True)
+    for _ in range(args.warmup):
+        flush.zero_()
+        fused()
+    barrier()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    step_ms, score_ms, kern_ms = [], [], []
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    for _ in range(args.steps):
+        flush.zero_()
+        ev0.record()
+        fused()
+        ev1.record()
+        ev1.synchronize()
+        step_ms.append(ev0.elapsed_time(ev1))
+        t = m.idx_topk_last_timings()
+        score_ms.append(t["score_ms"])
+        kern_ms.append(t["kernels_ms"])
+    barrier()
+    clk = clocks.stop()
+    total = torch.tensor([sum(step_ms)], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(total, op=dist.ReduceOp.MAX)
+    ms_per_step = float(total.item()) / args.steps
+    value = world * flop / (ms_per_step * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers (pinned), copies timed
+    pinned = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host.items()}
+    h_phys = torch.empty((R, K), dtype=torch.int32).pin_memory()
+    h_raw = torch.empty((R, K), dtype=torch.int32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = 2 * R * K * 4
+    e2e_ms = []
+    n_e2e = max(3, min(args.steps, 20))
+    for i in range(n_e2e + 2):
+        flush.zero_()
+        torch.cuda.synchronize()
+        ev0.record()
+        for k, v in pinned.items():
+            dev[k].copy_(v, non_blocking=True)
+        fused()
+        h_phys.copy_(phys, non_blocking=True)
+        h_raw.copy_(raw, non_blocking=True)
+        ev1.record()
+        ev1.synchronize()
+        if i >= 2:
+            e2e_ms.append(ev0.elapsed_time(ev1))
+    e2e_step = statistics.mean(e2e_ms)
+    m.idx_topk_set_timing(False)
+
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp4",
+            "data": "synthetic",
+            "config": {"workload": p.name, "rows": R, "c4_context": p.max_end(), "topk": K,
+                       "heads": 64, "dim": 128, "page": 64, "scored_pairs": p.scored_pairs(),
+                       "algorithmic_flop": flop,
+                       "l2": "flushed before every timed step (256 MiB write, untimed)",
+                       "parallelism": f"replicas x{world} (rows independent; no collective)"},
+            "gpu_launches": 4 * args.steps,
+            "clocks": clk,
+            "e2e": {"value": world * flop / (e2e_step * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "ms_per_step": e2e_step, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h}}
+
+    peaks, src = measured_peaks()
+    fp4_peak = float(peaks["bf16_tflops"]) * NOMINAL_FP4_OVER_BF16
+    sc = statistics.mean(score_ms)
+    achieved = flop / (sc * 1e-3) / 1e12
+    line["roofline"] = {"bound": "tensor", "achieved": achieved, "peak": fp4_peak,
+                        "unit": "TFLOP/s", "frac": achieved / fp4_peak,
+                        "traffic": ncu_traffic(p.name),
+                        "kernel": "score_kernel<select,%d>" % K, "kernel_ms": sc,
+                        "peak_source": f"{src} bf16 burst x {NOMINAL_FP4_OVER_BF16:g} "
+                                       "(nominal dense FP4/bf16 ratio)"}
+    line["phases_ms"] = {"kernels": statistics.mean(kern_ms), "score": sc}
+    line["scratch"] = {"bytes_per_call": m.idx_topk_fp4_scratch_bytes(R, K, local),
+                       "pool_high_water": m.idx_topk_scratch_high_water(local),
+                       "dense_scores_bytes": m.dense_score_bytes(R, p.max_end())}
+
+    if not args.no_dense:
+        ws = torch.empty((R, p.max_end()), dtype=torch.float32, device="cuda")
+        d_phys = torch.empty_like(phys)
+        d_raw = torch.empty_like(raw)
+
+        def dense():
+            m.idx_dense_topk_fp4_prefill(**dev, topk=K, out_phys_slot=d_phys, out_raw_idx=d_raw,
+                                         score_workspace=ws)
+
+        f_ms, d_ms = [], []
+        for i in range(5 + args.pairs):
+            for fn, acc in ((dense, d_ms), (fused, f_ms)):
+                flush.zero_()
+                ev0.record()
+                fn()
+                ev1.record()
+                ev1.synchronize()
+                if i >= 5:
+                    acc.append(ev0.elapsed_time(ev1))
+        same = bool(torch.equal(d_raw, raw) and torch.equal(d_phys, phys))
+        line["dense_topk"] = {"ms_median": statistics.median(d_ms),
+                              "fused_ms_median": statistics.median(f_ms),
+                              "speedup": statistics.median(d_ms) / statistics.median(f_ms),
+                              "pairs": args.pairs, "indices_identical": same,
+                              "score_storage_bytes": ws.numel() * 4}
+        del ws
+
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(p, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,158 @@
+"""GB300 (sm_103a) FP4 paged-MQA indexer prefill with fused exact TopK.
+
+Thin Python binding of the C ABI in include/idxtopk.h: every function below
+only marshals torch tensors into descriptors and calls the library of the same
+name on the caller's current CUDA stream; every step of the computation runs in
+the library's CUDA kernels.  There is no CPU fallback: a missing or unloadable
+library raises.
+
+The operation follows "[FlyDSL] Add FP4 LiteTopK prefill operator"
+(ROCm/aiter#5309) and "[FlyDSL][DSv4] Prototype FP4 MQA streaming TopK"
+(ROCm/aiter#5282): score every query row against its C4 window of the paged FP4
+K cache, score = sum_h w * ReLU(q_h . k), and return the exact TopK positions
+(physical slots and optional raw positions) without materialising the
+[rows, context] score matrix.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _lib
+
+__all__ = ["IdxError", "SUPPORTED_K", "idx_topk_fp4_prefill", "idx_dense_topk_fp4_prefill",
+           "idx_fp4_debug_scores", "idx_topk_select_scores", "idx_topk_supported_k",
+           "idx_topk_status_string", "idx_topk_fp4_scratch_bytes", "idx_topk_scratch_high_water",
+           "dense_score_bytes", "STATUS", "idx_topk_set_timing",
+           "idx_topk_last_timings"]
+
+STATUS = {0: "OK", 1: "INVALID_ARGUMENT", 2: "UNSUPPORTED", 3: "INVALID_METADATA",
+          4: "INVALID_PAGE", 5: "OVERFLOW", 6: "CUDA_ERROR", 7: "INTERNAL", 8: "TIMEOUT"}
+SUPPORTED_K = (512, 1024)
+
+_DT = {"uint8": 1, "int32": 2, "float32": 3}
+
+
+class IdxError(RuntimeError):
+    def __init__(self, code: int, fn: str):
+        self.code = int(code)
+        super().__init__(f"{fn}: {STATUS.get(code, code)} ({idx_topk_status_string(code)})")
+
+
+def _desc(t):
+    """idx_tensor_t descriptor of a torch tensor (no copy, no layout change)."""
+    if t is None:
+        return None
+    d = _lib.IdxTensor()
+    d.data = t.data_ptr() if t.numel() > 0 else None
+    d.dtype = _DT.get(str(t.dtype).replace("torch.", ""), 0)
+    d.ndim = t.dim()
+    for i in range(min(4, t.dim())):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _ref(d):
+    return ctypes.byref(d) if d is not None else None
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(code: int, fn: str, raise_on_error: bool):
+    if code != 0 and raise_on_error:
+        raise IdxError(code, fn)
+    return code
+
+
+def idx_topk_fp4_prefill(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                         row_start, row_end, topk, out_phys_slot, out_raw_idx=None, stream=None,
+                         raise_on_error=True) -> int:
+    """Fused scoring + exact TopK + page mapping; writes the outputs in place."""
+    lib = _lib.load()
+    ds = [_desc(t) for t in (q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                             row_start, row_end, out_phys_slot, out_raw_idx)]
+    code = lib.idx_topk_fp4_prefill(*[_ref(d) for d in ds[:9]], int(topk), _ref(ds[9]),
+                                    _ref(ds[10]), _stream(stream))
+    return _check(code, "idx_topk_fp4_prefill", raise_on_error)
+
+
+def idx_dense_topk_fp4_prefill(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                               row_start, row_end, topk, out_phys_slot, out_raw_idx=None,
+                               score_workspace=None, stream=None, raise_on_error=True) -> int:
+    """Comparison path: materialised fp32 scores, then a separate TopK."""
+    lib = _lib.load()
+    ds = [_desc(t) for t in (q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                             row_start, row_end, out_phys_slot, out_raw_idx, score_workspace)]
+    code = lib.idx_dense_topk_fp4_prefill(*[_ref(d) for d in ds[:9]], int(topk), _ref(ds[9]),
+                                          _ref(ds[10]), _ref(ds[11]), _stream(stream))
+    return _check(code, "idx_dense_topk_fp4_prefill", raise_on_error)
+
+
+def idx_fp4_debug_scores(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                         row_start, row_end, out_scores, out_logits=None, stream=None,
+                         raise_on_error=True) -> int:
+    """Scores (and optionally per-head logits) from the same scoring kernel."""
+    lib = _lib.load()
+    ds = [_desc(t) for t in (q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                             row_start, row_end, out_scores, out_logits)]
+    code = lib.idx_fp4_debug_scores(*[_ref(d) for d in ds], _stream(stream))
+    return _check(code, "idx_fp4_debug_scores", raise_on_error)
+
+
+def idx_topk_select_scores(scores, row_start, row_end, topk, out_raw_idx, stream=None,
+                           raise_on_error=True) -> int:
+    """Exact TopK of a materialised fp32 score matrix under the total order."""
+    lib = _lib.load()
+    ds = [_desc(t) for t in (scores, row_start, row_end, out_raw_idx)]
+    code = lib.idx_topk_select_scores(_ref(ds[0]), _ref(ds[1]), _ref(ds[2]), int(topk),
+                                      _ref(ds[3]), _stream(stream))
+    return _check(code, "idx_topk_select_scores", raise_on_error)
+
+
+def idx_topk_supported_k():
+    lib = _lib.load()
+    ptr = ctypes.POINTER(ctypes.c_int32)()
+    n = ctypes.c_int32(0)
+    code = lib.idx_topk_supported_k(ctypes.byref(ptr), ctypes.byref(n))
+    _check(code, "idx_topk_supported_k", True)
+    return tuple(ptr[i] for i in range(n.value))
+
+
+def idx_topk_status_string(code: int) -> str:
+    return _lib.load().idx_topk_status_string(int(code)).decode()
+
+
+def idx_topk_fp4_scratch_bytes(rows: int, topk: int, device: int = 0) -> int:
+    v = ctypes.c_uint64(0)
+    code = _lib.load().idx_topk_fp4_scratch_bytes(int(rows), int(topk), int(device),
+                                                  ctypes.byref(v))
+    _check(code, "idx_topk_fp4_scratch_bytes", True)
+    return int(v.value)
+
+
+def idx_topk_scratch_high_water(device: int = 0) -> int:
+    v = ctypes.c_uint64(0)
+    code = _lib.load().idx_topk_scratch_high_water(int(device), ctypes.byref(v))
+    _check(code, "idx_topk_scratch_high_water", True)
+    return int(v.value)
+
+
+def idx_topk_set_timing(enable: bool) -> None:
+    _lib.load().idx_topk_set_timing(1 if enable else 0)
+
+
+def idx_topk_last_timings() -> dict:
+    """Kernel-phase times (ms) of this thread's last call, when timing is on."""
+    buf = (ctypes.c_float * 4)()
+    _lib.load().idx_topk_last_timings(buf)
+    return {"plan_ms": buf[0], "score_ms": buf[1], "finish_ms": buf[2], "kernels_ms": buf[3]}
+
+
+def dense_score_bytes(rows: int, context: int) -> int:
+    """Bytes of the materialised fp32 [rows, context] score matrix of the dense path."""
+    return int(rows) * int(context) * 4

@@ -1,0 +1,113 @@
+"""Build and load the in-tree CUDA library libidxtopk.so (sm_103a).
+
+build() compiles the translation units under csrc/ in parallel with nvcc and
+links one shared library next to this file (git-ignored).  load() opens it
+with ctypes and declares the C ABI of include/idxtopk.h.  There is no fallback:
+if the library cannot be built or loaded, load() raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import shutil
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_HERE)
+CSRC = os.path.join(_HERE, "csrc")
+INCLUDE = os.path.join(_ROOT, "include")
+BUILD_DIR = os.path.join(_HERE, "_build")
+LIB_PATH = os.path.join(_HERE, "libidxtopk.so")
+SOURCES = ["host.cu", "plan.cu", "score.cu", "finish.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
+              "-I" + INCLUDE, "-I" + CSRC] + ARCH
+
+_lock = threading.Lock()
+_lib = None
+
+
+def _nvcc() -> str:
+    for cand in (shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: cannot build the sm_103a library")
+
+
+def _deps_mtime() -> float:
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    files.append(os.path.join(INCLUDE, "idxtopk.h"))
+    return max(os.path.getmtime(f) for f in files)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile csrc/*.cu for sm_103a and link libidxtopk.so (no-op when fresh)."""
+    if (not force and os.path.exists(LIB_PATH)
+            and os.path.getmtime(LIB_PATH) >= _deps_mtime()):
+        return LIB_PATH
+    nvcc = _nvcc()
+    os.makedirs(BUILD_DIR, exist_ok=True)
+
+    def compile_one(src: str) -> str:
+        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        cmd = [nvcc] + NVCC_FLAGS + ["-c", os.path.join(CSRC, src), "-o", obj]
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        if res.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {src}:\n{res.stderr}")
+        if verbose and res.stderr:
+            print(res.stderr)
+        return obj
+
+    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        objs = list(ex.map(compile_one, SOURCES))
+    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    cmd = [nvcc, "-shared"] + ARCH + objs + ["-o", tmp]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError(f"link failed:\n{res.stderr}")
+    os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+class IdxTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+EXPORTS = {
+    "idx_topk_fp4_prefill": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
+                             [ctypes.c_int32, ctypes.POINTER(IdxTensor), ctypes.POINTER(IdxTensor),
+                              ctypes.c_void_p]),
+    "idx_dense_topk_fp4_prefill": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
+                                   [ctypes.c_int32] + [ctypes.POINTER(IdxTensor)] * 3 +
+                                   [ctypes.c_void_p]),
+    "idx_fp4_debug_scores": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 11 + [ctypes.c_void_p]),
+    "idx_topk_select_scores": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 3 +
+                               [ctypes.c_int32, ctypes.POINTER(IdxTensor), ctypes.c_void_p]),
+    "idx_topk_supported_k": (ctypes.c_int, [ctypes.POINTER(ctypes.POINTER(ctypes.c_int32)),
+                                            ctypes.POINTER(ctypes.c_int32)]),
+    "idx_topk_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "idx_topk_fp4_scratch_bytes": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                  ctypes.POINTER(ctypes.c_uint64)]),
+    "idx_topk_scratch_high_water": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(ctypes.c_uint64)]),
+    "idx_topk_set_timing": (ctypes.c_int, [ctypes.c_int32]),
+    "idx_topk_last_timings": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float)]),
+}
+
+
+def load(path: str = None):
+    """Build if needed, then open the library and declare its C ABI."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        lib = ctypes.CDLL(path or build())
+        for name, (res, args) in EXPORTS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib

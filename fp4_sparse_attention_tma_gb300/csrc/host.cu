@@ -1,0 +1,669 @@
+// C ABI of the library (declared in include/idxtopk.h): argument validation,
+// device guard, graph-capture rejection, stream-ordered bounded scratch, TMA
+// descriptors, the kernel sequence, status read-back and fail-closed output
+// fill.  Follows the operator contract of "[FlyDSL] Add FP4 LiteTopK prefill
+// operator" (ROCm/aiter#5309, Implementation) and "[FlyDSL][DSv4] Prototype FP4
+// MQA streaming TopK" (ROCm/aiter#5282, Changes and Scope).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "idx_internal.h"
+#include "idx_launch.h"
+#include "idxtopk.h"
+
+using namespace idxk;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool init = false;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  cudaMemPool_t pool = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+// Optional per-kernel timing of the last call (CUDA events on the caller's
+// stream around each launch): plan+page check, scorer, finish, whole call.
+bool g_timing = false;
+thread_local float g_last_ms[4] = {0.f, 0.f, 0.f, 0.f};
+
+struct CallTimer {
+  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+  bool on = false;
+  CallTimer() {
+    if (!g_timing) return;
+    on = true;
+    for (auto& e : ev)
+      if (cudaEventCreate(&e) != cudaSuccess) on = false;
+  }
+  ~CallTimer() {
+    for (auto& e : ev)
+      if (e) cudaEventDestroy(e);
+  }
+  void mark(int i, cudaStream_t s) {
+    if (on) cudaEventRecord(ev[i], s);
+  }
+  // call after the stream has been synchronised
+  void collect(cudaEvent_t end) {
+    if (!on) return;
+    float t[4] = {0.f, 0.f, 0.f, 0.f};
+    cudaEvent_t pts[5] = {ev[0], ev[1], ev[2], ev[3], end};
+    for (int i = 0; i < 3; ++i) cudaEventElapsedTime(&t[i], pts[i], pts[i + 1]);
+    cudaEventElapsedTime(&t[3], pts[0], pts[3]);
+    for (int i = 0; i < 4; ++i) g_last_ms[i] = t[i];
+    cudaGetLastError();
+  }
+};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int device_state(int dev, DeviceState** out) {
+  if (dev < 0 || dev >= kMaxDevices) return IDX_ERR_INVALID_ARGUMENT;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.init) {
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return IDX_ERR_CUDA;
+    }
+    cudaMemPoolProps props;
+    memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    if (cudaMemPoolCreate(&d.pool, &props) != cudaSuccess) {
+      cudaGetLastError();
+      return IDX_ERR_CUDA;
+    }
+    uint64_t keep = UINT64_MAX;  // keep freed scratch reserved for the next call
+    cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    d.init = true;
+  }
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr) {
+      cudaGetLastError();
+      return IDX_ERR_CUDA;
+    }
+    g_encode = (EncodeTiledFn)fn;
+  }
+  *out = &d;
+  return IDX_OK;
+}
+
+// ---------------------------------------------------------- validation ----
+
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+  if (a < 0 || b < 0) return false;
+  if (a != 0 && b > INT64_MAX / a) return false;
+  *out = a * b;
+  return true;
+}
+
+// Validates one descriptor: dtype, rank, non-negative shape, C-contiguous
+// strides, 16-byte aligned base (unless empty).  Returns IDX_OK or an error.
+int check_tensor(const idx_tensor_t* t, int dtype, int ndim) {
+  if (!t) return IDX_ERR_INVALID_ARGUMENT;
+  if (t->dtype != dtype || t->ndim != ndim) return IDX_ERR_INVALID_ARGUMENT;
+  int64_t numel = 1;
+  for (int i = 0; i < ndim; ++i) {
+    if (t->shape[i] < 0) return IDX_ERR_INVALID_ARGUMENT;
+    if (!mul_ok(numel, t->shape[i], &numel)) return IDX_ERR_OVERFLOW;
+  }
+  int64_t expect = 1;
+  for (int i = ndim - 1; i >= 0; --i) {
+    if (t->shape[i] > 1 && t->stride[i] != expect) return IDX_ERR_INVALID_ARGUMENT;
+    if (!mul_ok(expect, t->shape[i] > 0 ? t->shape[i] : 1, &expect)) return IDX_ERR_OVERFLOW;
+  }
+  int64_t bytes;
+  if (!mul_ok(numel, dtype == IDX_U8 ? 1 : 4, &bytes)) return IDX_ERR_OVERFLOW;
+  if (numel > 0) {
+    if (!t->data) return IDX_ERR_INVALID_ARGUMENT;
+    if (((uintptr_t)t->data & 15u) != 0) return IDX_ERR_INVALID_ARGUMENT;
+  }
+  return IDX_OK;
+}
+
+int64_t numel_of(const idx_tensor_t* t) {
+  int64_t n = 1;
+  for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
+  return n;
+}
+
+// Device that owns `ptr` (device or managed memory), or -1.
+int device_of(const void* ptr) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return -1;
+  return a.device;
+}
+
+class DeviceGuard {
+ public:
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev_) != cudaSuccess) {
+      cudaGetLastError();
+      prev_ = -1;
+    }
+    if (prev_ != dev) ok_ = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (prev_ >= 0) cudaSetDevice(prev_);
+  }
+  bool ok() const { return ok_; }
+
+ private:
+  int prev_ = -1;
+  bool ok_ = true;
+};
+
+struct Outputs {
+  const idx_tensor_t* t[2] = {nullptr, nullptr};
+};
+
+// Fills valid outputs with -1 on `stream` and waits for it.
+void fill_minus_one(const Outputs& o, cudaStream_t stream) {
+  for (const idx_tensor_t* t : o.t) {
+    if (!t) continue;
+    const int64_t n = numel_of(t);
+    if (n > 0) cudaMemsetAsync(t->data, 0xFF, (size_t)n * 4, stream);
+  }
+  cudaStreamSynchronize(stream);
+  cudaGetLastError();
+}
+
+// Common checks of the scoring inputs; on success fills the sizes.
+struct Sizes {
+  int64_t rows = 0, num_pages = 0, num_req = 0, max_pages = 0;
+};
+
+int check_inputs(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                 const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
+                 const idx_tensor_t* weights, const idx_tensor_t* page_table,
+                 const idx_tensor_t* row_req, const idx_tensor_t* row_start,
+                 const idx_tensor_t* row_end, Sizes* sz) {
+  int st;
+  if ((st = check_tensor(q_fp4, IDX_U8, 3))) return st;
+  if ((st = check_tensor(q_scale, IDX_U8, 3))) return st;
+  if ((st = check_tensor(k_cache_fp4, IDX_U8, 3))) return st;
+  if ((st = check_tensor(k_scale, IDX_U8, 3))) return st;
+  if ((st = check_tensor(weights, IDX_F32, 2))) return st;
+  if ((st = check_tensor(page_table, IDX_I32, 2))) return st;
+  if ((st = check_tensor(row_req, IDX_I32, 1))) return st;
+  if ((st = check_tensor(row_start, IDX_I32, 1))) return st;
+  if ((st = check_tensor(row_end, IDX_I32, 1))) return st;
+  // H = 64 heads, D = 128 (64 bytes, 4 scales), page size 64 are the supported
+  // specialisation (aiter#5282 Scope)
+  if (q_fp4->shape[1] != kHeads || q_fp4->shape[2] != kDimBytes) return IDX_ERR_UNSUPPORTED;
+  if (k_cache_fp4->shape[1] != kPage || k_cache_fp4->shape[2] != kDimBytes) return IDX_ERR_UNSUPPORTED;
+  const int64_t R = q_fp4->shape[0];
+  if (q_scale->shape[0] != R || q_scale->shape[1] != kHeads || q_scale->shape[2] != kNumSF)
+    return IDX_ERR_INVALID_ARGUMENT;
+  if (k_scale->shape[0] != k_cache_fp4->shape[0] || k_scale->shape[1] != kPage ||
+      k_scale->shape[2] != kNumSF)
+    return IDX_ERR_INVALID_ARGUMENT;
+  if (weights->shape[0] != R || weights->shape[1] != kHeads) return IDX_ERR_INVALID_ARGUMENT;
+  if (row_req->shape[0] != R || row_start->shape[0] != R || row_end->shape[0] != R)
+    return IDX_ERR_INVALID_ARGUMENT;
+  sz->rows = R;
+  sz->num_pages = k_cache_fp4->shape[0];
+  sz->num_req = page_table->shape[0];
+  sz->max_pages = page_table->shape[1];
+  // physical slots and logical positions are int32 (aiter#5309 Implementation:
+  // 64-bit addressing inside, overflow rejected at the int32 outputs)
+  if (R > INT32_MAX || sz->num_pages * (int64_t)kPage > INT32_MAX ||
+      sz->max_pages * (int64_t)kPage > INT32_MAX || sz->num_req > INT32_MAX ||
+      R * (int64_t)kHeads > INT32_MAX)
+    return IDX_ERR_OVERFLOW;
+  if (R > 0 && (sz->num_pages < 1 || sz->num_req < 1 || sz->max_pages < 1))
+    return IDX_ERR_INVALID_ARGUMENT;
+  return IDX_OK;
+}
+
+int check_output(const idx_tensor_t* out, int64_t rows, int32_t topk) {
+  int st = check_tensor(out, IDX_I32, 2);
+  if (st) return st;
+  if (out->shape[0] != rows || out->shape[1] != topk) return IDX_ERR_INVALID_ARGUMENT;
+  return IDX_OK;
+}
+
+bool topk_supported(int32_t k) { return k == 512 || k == 1024; }
+
+// Every non-empty tensor must be device memory of one device; returns it.
+int common_device(const idx_tensor_t* const* ts, int n, int* dev) {
+  int d = -1;
+  for (int i = 0; i < n; ++i) {
+    const idx_tensor_t* t = ts[i];
+    if (!t || numel_of(t) == 0) continue;
+    const int td = device_of(t->data);
+    if (td < 0) return IDX_ERR_INVALID_ARGUMENT;
+    if (d >= 0 && td != d) return IDX_ERR_INVALID_ARGUMENT;
+    d = td;
+  }
+  if (d < 0 && cudaGetDevice(&d) != cudaSuccess) {
+    cudaGetLastError();
+    return IDX_ERR_CUDA;
+  }
+  *dev = d;
+  return IDX_OK;
+}
+
+int check_stream(cudaStream_t stream, int dev) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return IDX_ERR_CUDA;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return IDX_ERR_UNSUPPORTED;
+  if (stream != nullptr) {
+    int sd = -1;
+    if (cudaStreamGetDevice(stream, &sd) != cudaSuccess) {
+      cudaGetLastError();
+      return IDX_ERR_INVALID_ARGUMENT;
+    }
+    if (sd != dev) return IDX_ERR_INVALID_ARGUMENT;
+  }
+  return IDX_OK;
+}
+
+int encode_2d_u8(CUtensorMap* map, void* base, uint64_t rows, uint32_t box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)kDimBytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kDimBytes};
+  cuuint32_t box[2] = {(cuuint32_t)kDimBytes, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? IDX_OK : IDX_ERR_CUDA;
+}
+
+struct Scratch {
+  void* base = nullptr;
+  ScratchLayout L{};
+  PlanHeader* hdr() const { return (PlanHeader*)((char*)base + L.header); }
+  template <typename T>
+  T* at(size_t off) const {
+    return (T*)((char*)base + off);
+  }
+};
+
+enum class Path { kFused, kDense, kDebug };
+
+struct Call {
+  const idx_tensor_t *q_fp4, *q_scale, *k_cache_fp4, *k_scale, *weights, *page_table, *row_req,
+      *row_start, *row_end;
+  int32_t topk;
+  const idx_tensor_t *out_phys, *out_raw;   // prefill outputs
+  const idx_tensor_t *scores, *logits;      // dense / debug score outputs
+  Path path;
+};
+
+int read_status_and_free(const Scratch& s, cudaStream_t stream, uint32_t* status) {
+  // pageable destination: returns once the copy (and all earlier work on the
+  // stream) has completed
+  cudaError_t e1 = cudaMemcpyAsync(status, s.hdr(), sizeof(uint32_t), cudaMemcpyDeviceToHost, stream);
+  cudaError_t e2 = cudaFreeAsync(s.base, stream);
+  if (e1 != cudaSuccess || e2 != cudaSuccess) {
+    cudaGetLastError();
+    return IDX_ERR_CUDA;
+  }
+  return IDX_OK;
+}
+
+int run(const Call& c, cudaStream_t stream) {
+  Outputs outs;
+  const bool prefill = c.path != Path::kDebug;
+  // outputs first, so that later errors can fail closed
+  int64_t rows_hint = c.q_fp4 ? c.q_fp4->shape[0] : 0;
+  if (prefill) {
+    int st = check_output(c.out_phys, rows_hint, c.topk);
+    if (st) return st;
+    outs.t[0] = c.out_phys;
+    if (c.out_raw) {
+      st = check_output(c.out_raw, rows_hint, c.topk);
+      if (st) return st;
+      outs.t[1] = c.out_raw;
+    }
+  }
+  const idx_tensor_t* all[] = {c.q_fp4, c.q_scale, c.k_cache_fp4, c.k_scale, c.weights, c.page_table,
+                               c.row_req, c.row_start, c.row_end, c.out_phys, c.out_raw,
+                               c.scores, c.logits};
+  int dev = -1;
+  int st = common_device(all, 13, &dev);
+  if (st) return st;
+  DeviceGuard guard(dev);
+  if (!guard.ok()) return IDX_ERR_CUDA;
+  st = check_stream(stream, dev);
+  if (st == IDX_ERR_UNSUPPORTED) return st;  // capturing: enqueue nothing
+  auto fail = [&](int code) {
+    fill_minus_one(outs, stream);
+    return code;
+  };
+  if (st) return fail(st);
+  if (prefill && !topk_supported(c.topk)) return fail(IDX_ERR_UNSUPPORTED);
+  Sizes sz;
+  st = check_inputs(c.q_fp4, c.q_scale, c.k_cache_fp4, c.k_scale, c.weights, c.page_table,
+                    c.row_req, c.row_start, c.row_end, &sz);
+  if (st) return fail(st);
+  int64_t score_stride = 0, logits_stride = 0, check_end = 0;
+  if (c.path != Path::kFused && c.scores) {
+    if ((st = check_tensor(c.scores, IDX_F32, 2))) return fail(st);
+    if (c.scores->shape[0] != sz.rows) return fail(IDX_ERR_INVALID_ARGUMENT);
+    score_stride = c.scores->shape[1];
+    if (score_stride > INT32_MAX) return fail(IDX_ERR_OVERFLOW);
+    check_end = score_stride;
+  }
+  if (c.path == Path::kDebug) {
+    if (!c.scores) return fail(IDX_ERR_INVALID_ARGUMENT);
+    if (c.logits) {
+      if ((st = check_tensor(c.logits, IDX_F32, 3))) return fail(st);
+      if (c.logits->shape[0] != sz.rows || c.logits->shape[1] != kHeads)
+        return fail(IDX_ERR_INVALID_ARGUMENT);
+      logits_stride = c.logits->shape[2];
+      if (logits_stride < check_end) check_end = logits_stride;
+    }
+  }
+  if (sz.rows == 0) return IDX_OK;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(dev, &ds))) return fail(st);
+  if (!(ds->cc_major == 10 && ds->cc_minor == 3)) return fail(IDX_ERR_UNSUPPORTED);
+
+  const int grid = ds->sm_count;
+  const bool with_cands = c.path == Path::kFused;
+  Scratch s;
+  s.L = scratch_layout(sz.rows, c.topk, grid, with_cands);
+  // the dense path without a caller workspace materialises [rows, max_pages*64]
+  size_t ws_off = 0;
+  size_t total = s.L.total;
+  if (c.path == Path::kDense && !c.scores) {
+    int64_t width = sz.max_pages * kPage, bytes;
+    if (!mul_ok(sz.rows, width, &bytes) || !mul_ok(bytes, 4, &bytes)) return fail(IDX_ERR_OVERFLOW);
+    ws_off = align_up(total, 256);
+    total = ws_off + (size_t)bytes;
+    score_stride = width;
+    check_end = width;
+  }
+  if (cudaMallocFromPoolAsync(&s.base, total, ds->pool, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(IDX_ERR_CUDA);
+  }
+  cudaMemsetAsync(s.hdr(), 0, sizeof(PlanHeader), stream);
+  float* score_buf = nullptr;
+  if (c.path != Path::kFused)
+    score_buf = c.scores ? (float*)c.scores->data : s.at<float>(ws_off);
+
+  PlanParams pp{};
+  pp.row_req = (const int32_t*)c.row_req->data;
+  pp.row_start = (const int32_t*)c.row_start->data;
+  pp.row_end = (const int32_t*)c.row_end->data;
+  pp.page_table = (const int32_t*)c.page_table->data;
+  pp.rows = (int32_t)sz.rows;
+  pp.num_req = (int32_t)sz.num_req;
+  pp.max_pages = (int32_t)sz.max_pages;
+  pp.num_pages = (int32_t)sz.num_pages;
+  pp.score_thr = c.path == Path::kDebug ? 0 : c.topk;
+  pp.grid = grid;
+  pp.check_end_le = c.path == Path::kFused ? -1 : (int32_t)check_end;
+  pp.max_units = s.L.max_units;
+  pp.max_row_slots = s.L.max_row_slots;
+  pp.hdr = s.hdr();
+  pp.row_block = s.at<int32_t>(s.L.row_block);
+  pp.blocks = s.at<BlockInfo>(s.L.blocks);
+  pp.units = s.at<UnitInfo>(s.L.units);
+  pp.sched = s.at<int32_t>(s.L.sched);
+  int cuda_err = 0;
+  CallTimer timer;
+  timer.mark(0, stream);
+  cuda_err |= launch_plan(pp, stream) != cudaSuccess;
+
+  CUtensorMap tmap_k, tmap_q;
+  if (encode_2d_u8(&tmap_k, c.k_cache_fp4->data, (uint64_t)sz.num_pages * kPage, kPage) ||
+      encode_2d_u8(&tmap_q, c.q_fp4->data, (uint64_t)sz.rows * kHeads, kRowsPerChunk * kHeads)) {
+    uint32_t dummy;
+    read_status_and_free(s, stream, &dummy);
+    return fail(IDX_ERR_CUDA);
+  }
+  ScoreParams sp{};
+  sp.q_scale = (const uint8_t*)c.q_scale->data;
+  sp.k_scale = (const uint8_t*)c.k_scale->data;
+  sp.weights = (const float*)c.weights->data;
+  sp.page_table = pp.page_table;
+  sp.row_start = pp.row_start;
+  sp.row_end = pp.row_end;
+  sp.rows = pp.rows;
+  sp.max_pages = pp.max_pages;
+  sp.num_pages = pp.num_pages;
+  sp.topk = c.topk;
+  sp.mode = c.path == Path::kFused ? kModeSelect : kModeDense;
+  sp.score_thr = pp.score_thr;
+  sp.hdr = pp.hdr;
+  sp.blocks = pp.blocks;
+  sp.units = pp.units;
+  sp.sched = pp.sched;
+  sp.cand_cnt = with_cands ? s.at<uint32_t>(s.L.cand_cnt) : nullptr;
+  sp.cand_keys = with_cands ? s.at<uint64_t>(s.L.cand_keys) : nullptr;
+  sp.dense_out = score_buf;
+  sp.dense_stride = score_stride;
+  sp.logits_out = c.logits ? (float*)c.logits->data : nullptr;
+  sp.logits_stride = logits_stride;
+  timer.mark(1, stream);
+  cuda_err |= launch_score(tmap_k, tmap_q, sp, grid, stream) != cudaSuccess;
+  timer.mark(2, stream);
+
+  if (prefill) {
+    FinishParams fp{};
+    fp.row_req = pp.row_req;
+    fp.row_start = pp.row_start;
+    fp.row_end = pp.row_end;
+    fp.page_table = pp.page_table;
+    fp.rows = pp.rows;
+    fp.max_pages = pp.max_pages;
+    fp.topk = c.topk;
+    fp.hdr = pp.hdr;
+    fp.row_block = pp.row_block;
+    fp.blocks = pp.blocks;
+    fp.cand_cnt = sp.cand_cnt;
+    fp.cand_keys = sp.cand_keys;
+    fp.scores = c.path == Path::kDense ? score_buf : nullptr;
+    fp.score_stride = score_stride;
+    fp.out_phys = (int32_t*)c.out_phys->data;
+    fp.out_raw = c.out_raw ? (int32_t*)c.out_raw->data : nullptr;
+    cuda_err |= launch_finish(fp, stream) != cudaSuccess;
+  }
+  timer.mark(3, stream);
+  cudaEvent_t end_ev = nullptr;
+  if (timer.on && cudaEventCreate(&end_ev) == cudaSuccess) cudaEventRecord(end_ev, stream);
+  uint32_t status = 0;
+  st = read_status_and_free(s, stream, &status);
+  if (end_ev) {
+    timer.collect(end_ev);
+    cudaEventDestroy(end_ev);
+  }
+  if (cuda_err || st || cudaGetLastError() != cudaSuccess) return fail(IDX_ERR_CUDA);
+  if (status != kOk) return fail((int)status);
+  return IDX_OK;
+}
+
+const int32_t kSupportedK[2] = {512, 1024};
+
+}  // namespace
+
+extern "C" {
+
+int idx_topk_fp4_prefill(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                         const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
+                         const idx_tensor_t* weights, const idx_tensor_t* page_table,
+                         const idx_tensor_t* row_req, const idx_tensor_t* row_start,
+                         const idx_tensor_t* row_end, int32_t topk,
+                         const idx_tensor_t* out_phys_slot, const idx_tensor_t* out_raw_idx,
+                         idx_stream_t stream) {
+  Call c{q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req, row_start, row_end,
+         topk, out_phys_slot, out_raw_idx, nullptr, nullptr, Path::kFused};
+  return run(c, (cudaStream_t)stream);
+}
+
+int idx_dense_topk_fp4_prefill(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                               const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
+                               const idx_tensor_t* weights, const idx_tensor_t* page_table,
+                               const idx_tensor_t* row_req, const idx_tensor_t* row_start,
+                               const idx_tensor_t* row_end, int32_t topk,
+                               const idx_tensor_t* out_phys_slot,
+                               const idx_tensor_t* out_raw_idx,
+                               const idx_tensor_t* score_workspace, idx_stream_t stream) {
+  Call c{q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req, row_start, row_end,
+         topk, out_phys_slot, out_raw_idx, score_workspace, nullptr, Path::kDense};
+  return run(c, (cudaStream_t)stream);
+}
+
+int idx_fp4_debug_scores(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                         const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
+                         const idx_tensor_t* weights, const idx_tensor_t* page_table,
+                         const idx_tensor_t* row_req, const idx_tensor_t* row_start,
+                         const idx_tensor_t* row_end, const idx_tensor_t* out_scores,
+                         const idx_tensor_t* out_logits, idx_stream_t stream) {
+  Call c{q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req, row_start, row_end,
+         0, nullptr, nullptr, out_scores, out_logits, Path::kDebug};
+  return run(c, (cudaStream_t)stream);
+}
+
+int idx_topk_select_scores(const idx_tensor_t* scores, const idx_tensor_t* row_start,
+                           const idx_tensor_t* row_end, int32_t topk,
+                           const idx_tensor_t* out_raw_idx, idx_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  int st = check_tensor(scores, IDX_F32, 2);
+  if (st) return st;
+  const int64_t R = scores->shape[0];
+  if ((st = check_output(out_raw_idx, R, topk))) return st;
+  Outputs outs;
+  outs.t[0] = out_raw_idx;
+  const idx_tensor_t* all[] = {scores, row_start, row_end, out_raw_idx};
+  int dev = -1;
+  if ((st = common_device(all, 4, &dev))) return st;
+  DeviceGuard guard(dev);
+  if (!guard.ok()) return IDX_ERR_CUDA;
+  st = check_stream(stream, dev);
+  if (st == IDX_ERR_UNSUPPORTED) return st;
+  auto fail = [&](int code) {
+    fill_minus_one(outs, stream);
+    return code;
+  };
+  if (st) return fail(st);
+  if (!topk_supported(topk)) return fail(IDX_ERR_UNSUPPORTED);
+  if ((st = check_tensor(row_start, IDX_I32, 1)) || (st = check_tensor(row_end, IDX_I32, 1)))
+    return fail(st);
+  if (row_start->shape[0] != R || row_end->shape[0] != R) return fail(IDX_ERR_INVALID_ARGUMENT);
+  if (R > INT32_MAX || scores->shape[1] > INT32_MAX) return fail(IDX_ERR_OVERFLOW);
+  if (R == 0) return IDX_OK;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(dev, &ds))) return fail(st);
+  if (!(ds->cc_major == 10 && ds->cc_minor == 3)) return fail(IDX_ERR_UNSUPPORTED);
+  Scratch s;
+  s.L = scratch_layout(0, topk, 0, false);
+  if (cudaMallocFromPoolAsync(&s.base, s.L.total, ds->pool, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(IDX_ERR_CUDA);
+  }
+  cudaMemsetAsync(s.hdr(), 0, sizeof(PlanHeader), stream);
+  int cuda_err = 0;
+  cuda_err |= launch_validate_windows((const int32_t*)row_start->data, (const int32_t*)row_end->data,
+                                      (int32_t)R, scores->shape[1], s.hdr(), stream) != cudaSuccess;
+  FinishParams fp{};
+  fp.row_start = (const int32_t*)row_start->data;
+  fp.row_end = (const int32_t*)row_end->data;
+  fp.rows = (int32_t)R;
+  fp.topk = topk;
+  fp.hdr = s.hdr();
+  fp.scores = (const float*)scores->data;
+  fp.score_stride = scores->shape[1];
+  fp.out_raw = (int32_t*)out_raw_idx->data;
+  cuda_err |= launch_finish(fp, stream) != cudaSuccess;
+  uint32_t status = 0;
+  st = read_status_and_free(s, stream, &status);
+  if (cuda_err || st || cudaGetLastError() != cudaSuccess) return fail(IDX_ERR_CUDA);
+  if (status != kOk) return fail((int)status);
+  return IDX_OK;
+}
+
+int idx_topk_supported_k(const int32_t** ks, int32_t* n) {
+  if (!ks || !n) return IDX_ERR_INVALID_ARGUMENT;
+  *ks = kSupportedK;
+  *n = 2;
+  return IDX_OK;
+}
+
+const char* idx_topk_status_string(int code) {
+  switch (code) {
+    case IDX_OK: return "ok";
+    case IDX_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case IDX_ERR_UNSUPPORTED: return "unsupported";
+    case IDX_ERR_INVALID_METADATA: return "invalid row metadata";
+    case IDX_ERR_INVALID_PAGE: return "invalid page-table entry";
+    case IDX_ERR_OVERFLOW: return "size overflow";
+    case IDX_ERR_CUDA: return "CUDA error";
+    case IDX_ERR_INTERNAL: return "internal selector failure";
+    case IDX_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int idx_topk_fp4_scratch_bytes(int32_t rows, int32_t topk, int32_t device, uint64_t* bytes) {
+  if (!bytes || rows < 0) return IDX_ERR_INVALID_ARGUMENT;
+  if (!topk_supported(topk)) return IDX_ERR_UNSUPPORTED;
+  int sm = 0;
+  if (cudaDeviceGetAttribute(&sm, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+    cudaGetLastError();
+    return IDX_ERR_CUDA;
+  }
+  *bytes = (uint64_t)scratch_layout(rows, topk, sm, true).total;
+  return IDX_OK;
+}
+
+int idx_topk_set_timing(int32_t enable) {
+  g_timing = enable != 0;
+  return IDX_OK;
+}
+
+int idx_topk_last_timings(float* ms4) {
+  if (!ms4) return IDX_ERR_INVALID_ARGUMENT;
+  for (int i = 0; i < 4; ++i) ms4[i] = g_last_ms[i];
+  return IDX_OK;
+}
+
+int idx_topk_scratch_high_water(int32_t device, uint64_t* bytes) {
+  if (!bytes) return IDX_ERR_INVALID_ARGUMENT;
+  DeviceState* ds = nullptr;
+  int st = device_state(device, &ds);
+  if (st) return st;
+  uint64_t v = 0;
+  if (cudaMemPoolGetAttribute(ds->pool, cudaMemPoolAttrReservedMemHigh, &v) != cudaSuccess) {
+    cudaGetLastError();
+    return IDX_ERR_CUDA;
+  }
+  *bytes = v;
+  return IDX_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,122 @@
+// Bounded streaming exact TopK in shared memory, used by the fused scorer's
+// epilogue, the candidate merge and the dense-matrix TopK.
+//
+// A row keeps a buffer of 64-bit order keys (see order_key) that are >= its
+// threshold tau.  Threads append passing keys with warp-aggregated atomics;
+// when the count gets close to the capacity, the group runs a radix select
+// (8-bit digits, most significant first, with early exit) that finds a
+// threshold T with exactly topk keys >= T, compacts the buffer to those keys
+// and raises tau to T.  Because the composite key includes the logical index,
+// keys of one row are distinct and the selection is exact.  This follows the
+// design stated in "[FlyDSL][DSv4] Prototype FP4 MQA streaming TopK"
+// (ROCm/aiter#5282, Changes): scores stream through a bounded on-chip pool; a
+// four-byte score radix plus a four-byte logical-index radix implements the
+// total order.
+#pragma once
+
+#include "idx_device.cuh"
+
+namespace idxk {
+
+// Appends `key` when `pass`; returns true (on lane 0 only) when the count after
+// this warp's append exceeds `limit`.  buf has room for cap entries.
+__device__ __forceinline__ bool sel_append(uint64_t* buf, uint32_t* cnt, uint32_t cap,
+                                           uint32_t limit, bool pass, uint64_t key) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t m = __ballot_sync(0xffffffffu, pass);
+  bool over = false;
+  if (m) {
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(cnt, (uint32_t)__popc(m));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const uint32_t pos = base + (uint32_t)__popc(m & ((1u << lane) - 1u));
+    if (pass && pos < cap) buf[pos] = key;
+    over = (lane == 0) && (base + (uint32_t)__popc(m) > limit);
+  }
+  return over;
+}
+
+// Collective over NT threads (tid in [0, NT), named barrier bar_id): reduces
+// the buffer to exactly K keys (those >= the K-th largest) when it holds more.
+// The count and tau in shared memory are updated; all threads must call it
+// with the same buffer.  PER = CAP / NT keys per thread are staged in
+// registers during the compaction.
+template <int NT, int CAP>
+__device__ __noinline__ void sel_compact(uint64_t* buf, uint32_t* cnt_s, uint64_t* tau_s,
+                                         uint32_t* hist, uint32_t* bc, uint32_t K, int tid,
+                                         uint32_t bar_id, PlanHeader* hdr) {
+  const uint32_t n = *(volatile uint32_t*)cnt_s;
+  if (n <= K) return;
+  uint64_t prefix = 0, pmask = 0;
+  uint32_t need = K;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int b = tid; b < 256; b += NT) hist[b] = 0;
+    bar_sync(bar_id, NT);
+    for (uint32_t i = tid; i < n; i += NT) {
+      const uint64_t k = buf[i];
+      if ((k & pmask) == prefix) atomicAdd(&hist[(uint32_t)(k >> shift) & 255u], 1u);
+    }
+    bar_sync(bar_id, NT);
+    if (tid < 32) {
+      uint32_t c[8], sum = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        c[e] = hist[255 - 8 * tid - e];
+        sum += c[e];
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (tid >= o) incl += v;
+      }
+      uint32_t above = incl - sum;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (above < need && above + c[e] >= need) {
+          bc[0] = 255u - 8u * tid - e;
+          bc[1] = above;
+          bc[2] = c[e];
+        }
+        above += c[e];
+      }
+    }
+    bar_sync(bar_id, NT);
+    const uint32_t d = bc[0], ab = bc[1], cd = bc[2];
+    need -= ab;
+    prefix |= (uint64_t)d << shift;
+    pmask |= (uint64_t)0xffu << shift;
+    if (cd == need) break;
+  }
+  constexpr int PER = CAP / NT;
+  uint64_t v[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const uint32_t i = (uint32_t)(tid + e * NT);
+    v[e] = i < n ? buf[i] : 0ull;
+  }
+  if (tid == 0) bc[3] = 0;
+  bar_sync(bar_id, NT);
+  const int lane = tid & 31;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const bool keep = v[e] != 0ull && v[e] >= prefix;
+    const uint32_t m = __ballot_sync(0xffffffffu, keep);
+    if (m) {
+      uint32_t base = 0;
+      if (lane == 0) base = atomicAdd(&bc[3], (uint32_t)__popc(m));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      const uint32_t pos = base + (uint32_t)__popc(m & ((1u << lane) - 1u));
+      if (keep && pos < (uint32_t)CAP) buf[pos] = v[e];
+    }
+  }
+  bar_sync(bar_id, NT);
+  if (tid == 0) {
+    if (bc[3] != K) raise_status(hdr, kErrInternal, 200);
+    *cnt_s = K;
+    *tau_s = prefix;
+  }
+  bar_sync(bar_id, NT);
+}
+
+}  // namespace idxk

@@ -1,0 +1,309 @@
+// Planning kernels: row-metadata validation, row blocks, work units, the
+// unit schedule, and validation of every page-table entry a window covers --
+// all before any K-cache byte is loaded ("[FlyDSL] Add FP4 LiteTopK prefill
+// operator", ROCm/aiter#5309, Implementation: fail closed on invalid
+// metadata/pages; "[FlyDSL][DSv4] Prototype FP4 MQA streaming TopK",
+// ROCm/aiter#5282, Validation: empty windows, nonzero starts, speculative page
+// lookahead).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "idx_device.cuh"
+#include "idx_launch.h"
+
+namespace idxk {
+
+namespace {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kRowsPerThread = 8;
+constexpr int kSortMax = 8192;  // units sorted by length when at most this many
+
+template <typename T, typename Op>
+__device__ T block_scan_incl(T v, T* warp_tot, Op op, T identity) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    T u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v = op(v, u);
+  }
+  if (lane == 31) warp_tot[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    T w = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : identity;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      T u = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w = op(w, u);
+    }
+    warp_tot[lane] = w;
+  }
+  __syncthreads();
+  if (warp > 0) v = op(v, warp_tot[warp - 1]);
+  __syncthreads();
+  return v;
+}
+
+struct AddI64 {
+  __device__ int64_t operator()(int64_t a, int64_t b) const { return a + b; }
+};
+struct MaxI32 {
+  __device__ int32_t operator()(int32_t a, int32_t b) const { return a > b ? a : b; }
+};
+
+__global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
+  __shared__ int64_t s_tot64[32];
+  __shared__ int32_t s_tot32[32];
+  __shared__ int64_t s_carry_blocks;
+  __shared__ int32_t s_carry_seg;
+  extern __shared__ __align__(16) uint64_t s_sort[];
+  const int tid = threadIdx.x;
+  PlanHeader* hdr = p.hdr;
+
+  // 1. row metadata
+  for (int r = tid; r < p.rows; r += kPlanThreads) {
+    int32_t req = p.row_req[r], s = p.row_start[r], e = p.row_end[r];
+    bool ok = req >= 0 && req < p.num_req && s >= 0 && e >= s &&
+              (int64_t)e <= (int64_t)p.max_pages * kPage && (p.check_end_le < 0 || e <= p.check_end_le);
+    if (!ok) raise_status(hdr, kErrInvalidMetadata, 100);
+  }
+  __syncthreads();
+  if (read_status(hdr) != kOk) return;
+
+  // 2. row blocks: a block starts at a request change or every kRowsPerBlock
+  //    rows into a run of one request.
+  if (tid == 0) {
+    s_carry_blocks = 0;
+    s_carry_seg = 0;
+  }
+  __syncthreads();
+  for (int64_t base = 0; base < p.rows; base += (int64_t)kPlanThreads * kRowsPerThread) {
+    const int64_t r0 = base + (int64_t)tid * kRowsPerThread;
+    int32_t last_seg = -1;
+    for (int k = 0; k < kRowsPerThread; ++k) {
+      int64_t r = r0 + k;
+      if (r < p.rows && (r == 0 || p.row_req[r] != p.row_req[r - 1])) last_seg = (int32_t)r;
+    }
+    int32_t incl = block_scan_incl<int32_t>(last_seg, s_tot32, MaxI32(), -1);
+    int32_t excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if ((tid & 31) == 0) excl = (tid >> 5) > 0 ? s_tot32[(tid >> 5) - 1] : -1;
+    int32_t seg = excl >= 0 ? excl : s_carry_seg;
+    int64_t nstart = 0;
+    for (int k = 0; k < kRowsPerThread; ++k) {
+      int64_t r = r0 + k;
+      if (r >= p.rows) break;
+      if (r == 0 || p.row_req[r] != p.row_req[r - 1]) seg = (int32_t)r;
+      if (((r - seg) % kRowsPerBlock) == 0) ++nstart;
+    }
+    int64_t bincl = block_scan_incl<int64_t>(nstart, s_tot64, AddI64(), 0);
+    int64_t b = s_carry_blocks + bincl - nstart;
+    seg = excl >= 0 ? excl : s_carry_seg;
+    for (int k = 0; k < kRowsPerThread; ++k) {
+      int64_t r = r0 + k;
+      if (r >= p.rows) break;
+      if (r == 0 || p.row_req[r] != p.row_req[r - 1]) seg = (int32_t)r;
+      if (((r - seg) % kRowsPerBlock) == 0) {
+        BlockInfo bi{};
+        bi.row0 = (int32_t)r;
+        bi.req = p.row_req[r];
+        p.blocks[b] = bi;
+        ++b;
+      }
+      p.row_block[r] = (int32_t)(b - 1);
+    }
+    __syncthreads();
+    if (tid == kPlanThreads - 1) {
+      s_carry_blocks += bincl;
+      int64_t last = base + (int64_t)kPlanThreads * kRowsPerThread - 1;
+      if (last >= p.rows) last = p.rows - 1;
+      // segment start of the last row of this tile
+      int32_t sg = incl >= 0 ? incl : s_carry_seg;
+      (void)last;
+      s_carry_seg = sg;
+    }
+    __syncthreads();
+  }
+  const int64_t n_blocks = s_carry_blocks;
+  __syncthreads();
+
+  // 3. per-block extent and tiles over the scored rows
+  int64_t my_tiles = 0;
+  for (int64_t b = tid; b < n_blocks; b += kPlanThreads) {
+    BlockInfo bi = p.blocks[b];
+    int32_t next = (b + 1 < n_blocks) ? p.blocks[b + 1].row0 : p.rows;
+    bi.nrows = next - bi.row0;
+    int32_t lo = INT32_MAX, hi = 0;
+    for (int j = 0; j < bi.nrows; ++j) {
+      int32_t s = p.row_start[bi.row0 + j], e = p.row_end[bi.row0 + j];
+      if (e - s > p.score_thr) {
+        lo = min(lo, s);
+        hi = max(hi, e);
+      }
+    }
+    if (hi > 0 && lo < hi) {
+      bi.tile0 = lo / kTile;
+      bi.ntiles = (hi + kTile - 1) / kTile - bi.tile0;
+    } else {
+      bi.tile0 = 0;
+      bi.ntiles = 0;
+    }
+    my_tiles += bi.ntiles;
+    p.blocks[b] = bi;
+  }
+  int64_t tot_tiles = block_scan_incl<int64_t>(my_tiles, s_tot64, AddI64(), 0);
+  if (tid == kPlanThreads - 1) s_tot64[0] = tot_tiles;
+  __syncthreads();
+  tot_tiles = s_tot64[0];
+  __syncthreads();
+  int64_t target = (int64_t)kUnitsPerCta * p.grid;
+  int64_t unit_tiles = (tot_tiles + target - 1) / target;
+  if (unit_tiles < kMinUnitTiles) unit_tiles = kMinUnitTiles;
+
+  // 4. units per block and candidate row-slots (blocks handled in tiles of
+  //    kPlanThreads with a running carry)
+  __shared__ int64_t s_unit_carry, s_slot_carry;
+  if (tid == 0) {
+    s_unit_carry = 0;
+    s_slot_carry = 0;
+  }
+  __syncthreads();
+  for (int64_t base = 0; base < n_blocks; base += kPlanThreads) {
+    int64_t b = base + tid;
+    int64_t nu = 0, ns = 0;
+    BlockInfo bi{};
+    if (b < n_blocks) {
+      bi = p.blocks[b];
+      nu = bi.ntiles > 0 ? (bi.ntiles + unit_tiles - 1) / unit_tiles : 0;
+      ns = nu * bi.nrows;
+    }
+    int64_t u_incl = block_scan_incl<int64_t>(nu, s_tot64, AddI64(), 0);
+    int64_t u_first = s_unit_carry + u_incl - nu;
+    int64_t s_incl = block_scan_incl<int64_t>(ns, s_tot64, AddI64(), 0);
+    int64_t s_first = s_slot_carry + s_incl - ns;
+    if (b < n_blocks) {
+      if (u_first + nu > p.max_units || s_first + ns > p.max_row_slots) {
+        raise_status(hdr, kErrInternal, 110);
+      } else {
+        bi.n_units = (int32_t)nu;
+        bi.unit_first = (int32_t)u_first;
+        bi.slot0 = s_first;
+        p.blocks[b] = bi;
+        for (int64_t k = 0; k < nu; ++k) {
+          UnitInfo u;
+          u.block = (int32_t)b;
+          u.k = (int32_t)k;
+          u.t_begin = bi.tile0 + (int32_t)((k * bi.ntiles) / nu);
+          u.t_end = bi.tile0 + (int32_t)(((k + 1) * bi.ntiles) / nu);
+          p.units[u_first + k] = u;
+        }
+      }
+    }
+    __syncthreads();
+    if (tid == kPlanThreads - 1) {
+      s_unit_carry += u_incl;
+      s_slot_carry += s_incl;
+    }
+    __syncthreads();
+  }
+  const int64_t n_units = s_unit_carry;
+  if (read_status(hdr) != kOk) return;
+
+  // 5. schedule: longest units first (static round-robin over persistent CTAs)
+  if (n_units <= kSortMax) {
+    int64_t n2 = 1;
+    while (n2 < n_units) n2 <<= 1;
+    for (int64_t i = tid; i < n2; i += kPlanThreads) {
+      uint64_t key = 0;
+      if (i < n_units) {
+        UnitInfo u = p.units[i];
+        key = ((uint64_t)(uint32_t)(u.t_end - u.t_begin) << 32) | (uint64_t)(~(uint32_t)i);
+      }
+      s_sort[i] = key;
+    }
+    __syncthreads();
+    for (int64_t size = 2; size <= n2; size <<= 1) {
+      for (int64_t stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int64_t i = tid; i < n2 / 2; i += kPlanThreads) {
+          int64_t lo = 2 * i - (i & (stride - 1));
+          int64_t hi = lo + stride;
+          uint64_t a = s_sort[lo], c = s_sort[hi];
+          bool desc = (lo & size) == 0;
+          if (desc ? (a < c) : (a > c)) {
+            s_sort[lo] = c;
+            s_sort[hi] = a;
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int64_t i = tid; i < n_units; i += kPlanThreads)
+      p.sched[i] = (int32_t)(~(uint32_t)(s_sort[i] & 0xffffffffu));
+  } else {
+    for (int64_t i = tid; i < n_units; i += kPlanThreads) p.sched[i] = (int32_t)i;
+  }
+  if (tid == 0) {
+    hdr->n_blocks = (int32_t)n_blocks;
+    hdr->n_units = (int32_t)n_units;
+    hdr->unit_tiles = (int32_t)unit_tiles;
+    hdr->n_row_slots = s_slot_carry;
+  }
+}
+
+// One warp per row block: every page-table entry that some row's window
+// [start, end) touches must name a page in [0, num_pages).
+__global__ void __launch_bounds__(256) validate_pages_kernel(PlanParams p) {
+  PlanHeader* hdr = p.hdr;
+  if (read_status(hdr) != kOk) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int32_t n_blocks = hdr->n_blocks;
+  for (int64_t b = warp; b < n_blocks; b += nwarps) {
+    BlockInfo bi = p.blocks[b];
+    int32_t s[kRowsPerBlock], e[kRowsPerBlock];
+    int32_t lo = INT32_MAX, hi = 0;
+    for (int j = 0; j < kRowsPerBlock; ++j) {
+      s[j] = 0;
+      e[j] = 0;
+      if (j < bi.nrows) {
+        s[j] = p.row_start[bi.row0 + j];
+        e[j] = p.row_end[bi.row0 + j];
+        if (e[j] > s[j]) {
+          lo = min(lo, s[j]);
+          hi = max(hi, e[j]);
+        }
+      }
+    }
+    if (hi <= lo) continue;
+    const int32_t p0 = lo / kPage, p1 = (hi + kPage - 1) / kPage;
+    const int32_t* row_pt = p.page_table + (int64_t)bi.req * p.max_pages;
+    bool bad = false;
+    for (int32_t pg = p0 + lane; pg < p1; pg += 32) {
+      bool need = false;
+      for (int j = 0; j < kRowsPerBlock; ++j)
+        need |= (s[j] < (pg + 1) * kPage) && (e[j] > pg * kPage) && (e[j] > s[j]);
+      if (need) {
+        int32_t v = row_pt[pg];
+        bad |= (v < 0) || (v >= p.num_pages);
+      }
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) raise_status(hdr, kErrInvalidPage, 120);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
+  static const size_t kSortBytes = sizeof(uint64_t) * kSortMax;
+  cudaError_t err = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSortBytes);
+  if (err != cudaSuccess) return err;
+  plan_kernel<<<1, kPlanThreads, kSortBytes, stream>>>(p);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  int blocks = p.grid > 0 ? p.grid * 4 : 128;
+  validate_pages_kernel<<<blocks, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace idxk

@@ -1,0 +1,196 @@
+/*
+ * idxtopk.h -- C ABI of the GB300 (sm_103a) FP4 paged-MQA indexer prefill with
+ * fused exact TopK.
+ *
+ * The operation (defined by "[FlyDSL] Add FP4 LiteTopK prefill operator",
+ * ROCm/aiter#5309, Summary and Implementation, and "[FlyDSL][DSv4] Prototype
+ * FP4 MQA streaming TopK", ROCm/aiter#5282, Changes and Scope):
+ *
+ *   for every query row r of request req = row_req[r] and window
+ *   [start, end) = [row_start[r], row_end[r]) of logical C4 positions:
+ *     logit[r,h,s] = sum_{d<128} q[r,h,d] * k[s,d]        (FP4 E2M1, UE8M0/32)
+ *     score[r,s]   = sum_{h<64} w[r,h] * max(logit[r,h,s], 0)    (fp32)
+ *     raw[r]       = the topk positions s in [start, end) ranked by score
+ *                    descending, then position ascending; NaN ranks below
+ *                    every number and +0 above -0 (aiter#5282 Changes).  When
+ *                    end - start <= topk the row returns start..end-1 in
+ *                    order, padded with -1 (short-row contract, aiter#5282
+ *                    Changes).  The dense [rows, context] score matrix is
+ *                    never materialised (aiter#5309 Summary).
+ *     phys[r]      = page_table[req][raw / 64] * 64 + raw % 64; -1 stays -1
+ *                    (aiter#5282 Changes: raw C4 positions mapped through the
+ *                    page table; sglang#38101 Changes: physical slots and
+ *                    optional raw indices written in place).
+ *
+ * Conventions for every entry point:
+ *  - Tensors are passed as idx_tensor_t descriptors of DEVICE memory that the
+ *    caller owns; the library keeps no pointer after it returns.  All tensors
+ *    of a call must live on one device; the call makes that device current for
+ *    its duration and restores the caller's current device before returning
+ *    (aiter#5309 Implementation: caller device/stream ownership).
+ *  - Work is enqueued on the caller's `stream` only (never the legacy default
+ *    stream); the call returns after that stream has reached the end of the
+ *    call's work, because the status is read back to the host.  Scratch is
+ *    allocated stream-ordered on that stream from a library-owned pool and is
+ *    bounded by rows, topk and the SM count -- never by the context length
+ *    (aiter#5282 Changes, last paragraph).
+ *  - Every tensor must be C-contiguous with a 16-byte-aligned base address.
+ *  - Offsets are computed in 64 bits (aiter#5309 Implementation).
+ *  - Fail closed (aiter#5309 Implementation): any error returns a nonzero
+ *    code, and, when the output descriptors themselves are valid, the outputs
+ *    are filled with -1 -- except while the stream is being captured into a
+ *    CUDA graph, where nothing is enqueued and IDX_ERR_UNSUPPORTED is returned
+ *    (aiter#5282 Scope: graph capture is rejected explicitly).
+ */
+#ifndef IDXTOPK_H_
+#define IDXTOPK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st* idx_stream_t;
+
+typedef enum {
+  IDX_OK = 0,
+  IDX_ERR_INVALID_ARGUMENT = 1, /* null/misaligned/non-contiguous tensor, wrong dtype/rank/shape,
+                                   tensors on different devices */
+  IDX_ERR_UNSUPPORTED = 2,      /* topk not in {512, 1024}; H != 64, D != 128, page != 64;
+                                   stream capture active; device is not sm_103 */
+  IDX_ERR_INVALID_METADATA = 3, /* row_req out of [0, num_req), start < 0, end < start,
+                                   end > max_pages * 64 */
+  IDX_ERR_INVALID_PAGE = 4,     /* a page-table entry covering some row's window is outside
+                                   [0, num_pages) */
+  IDX_ERR_OVERFLOW = 5,         /* num_pages * 64 or max_pages * 64 exceeds INT32_MAX, or a
+                                   size product overflows 64 bits */
+  IDX_ERR_CUDA = 6,             /* a CUDA runtime/driver call failed */
+  IDX_ERR_INTERNAL = 7,         /* selector failure: a scored row produced fewer than topk
+                                   candidates, or a plan bound was exceeded */
+  IDX_ERR_TIMEOUT = 8           /* a bounded device-side wait expired (the kernel returned
+                                   instead of hanging) */
+} idx_status_t;
+
+typedef enum { IDX_U8 = 1, IDX_I32 = 2, IDX_F32 = 3 } idx_dtype_t;
+
+/* Descriptor of one device tensor.  shape/stride are in elements; only the
+ * first ndim entries are read. */
+typedef struct {
+  void* data;
+  int32_t dtype; /* idx_dtype_t */
+  int32_t ndim;
+  int64_t shape[4];
+  int64_t stride[4];
+} idx_tensor_t;
+
+/*
+ * Fused FP4 paged-MQA scoring + exact TopK + page mapping (the hot path).
+ *
+ *   q_fp4        u8  [R, 64, 64]   FP4 E2M1 codes of the 64x128 query block of each row,
+ *                                  two per byte, even element of D in the low nibble
+ *   q_scale      u8  [R, 64, 4]    UE8M0 scale per 32 elements of D (2^(byte-127))
+ *   k_cache_fp4  u8  [NP, 64, 64]  C4 K cache, page size 64, same encoding
+ *   k_scale      u8  [NP, 64, 4]   UE8M0 scales of the K cache
+ *   weights      f32 [R, 64]       per-head weights
+ *   page_table   i32 [NR, MP]      physical page of logical page p of request i
+ *   row_req      i32 [R]           request of each row
+ *   row_start    i32 [R]           window start (logical C4 position, inclusive)
+ *   row_end      i32 [R]           window end (exclusive)
+ *   topk         512 or 1024
+ *   out_phys_slot i32 [R, topk]    physical C4 slot (page * 64 + offset) or -1
+ *   out_raw_idx   i32 [R, topk]    logical C4 position or -1; may be NULL
+ *
+ * Rows whose window is longer than topk are ordered by (score desc, position asc).
+ * Scale bytes of 255 (NaN) are outside the contract.
+ */
+int idx_topk_fp4_prefill(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                         const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
+                         const idx_tensor_t* weights, const idx_tensor_t* page_table,
+                         const idx_tensor_t* row_req, const idx_tensor_t* row_start,
+                         const idx_tensor_t* row_end, int32_t topk,
+                         const idx_tensor_t* out_phys_slot, const idx_tensor_t* out_raw_idx,
+                         idx_stream_t stream);
+
+/* The supported topk values, {512, 1024} (aiter#5309 Implementation: explicit
+ * supported-K contract).  *ks points to static storage.  Always IDX_OK unless
+ * an argument is NULL (IDX_ERR_INVALID_ARGUMENT). */
+int idx_topk_supported_k(const int32_t** ks, int32_t* n);
+
+/* Static, human-readable name of a status code. */
+const char* idx_topk_status_string(int code);
+
+/* Scratch bytes that idx_topk_fp4_prefill allocates for `rows` rows and
+ * `topk`, on `device` (its SM count bounds the work units).  Independent of
+ * the context length (aiter#5282 Changes, last paragraph; sglang#38101 Memory
+ * geometry).  Returns IDX_ERR_UNSUPPORTED for an unsupported topk,
+ * IDX_ERR_CUDA if the device cannot be queried. */
+int idx_topk_fp4_scratch_bytes(int32_t rows, int32_t topk, int32_t device, uint64_t* bytes);
+
+/* Peak bytes ever reserved by the library's scratch pool on `device` in this
+ * process (the pool's reserved-memory high-water mark). */
+int idx_topk_scratch_high_water(int32_t device, uint64_t* bytes);
+
+/* Measurement support (no counterpart on the pages): when enabled, each call
+ * of the calling thread records CUDA events on its stream around the kernel
+ * phases; idx_topk_last_timings then returns, in milliseconds, {planning and
+ * page validation, scoring kernel, finishing kernel, whole kernel sequence} of
+ * that thread's last completed call.  Process-wide switch; default off. */
+int idx_topk_set_timing(int32_t enable);
+int idx_topk_last_timings(float* ms4);
+
+/*
+ * Debug / dense scorer: the same scoring kernel as the fused path, writing the
+ * fp32 scores instead of selecting.
+ *   out_scores f32 [R, S]      score[r, s] written for every s in [start_r, end_r)
+ *                              of every row with a non-empty window; other entries are
+ *                              left untouched.  S >= max(row_end) is required and
+ *                              checked on the device (IDX_ERR_INVALID_METADATA).
+ *   out_logits f32 [R, 64, S2] optional (may be NULL): per-head logits
+ *                              logit[r, h, s] for the same (r, s).
+ * Other arguments as for idx_topk_fp4_prefill (no topk, no outputs).
+ */
+int idx_fp4_debug_scores(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                         const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
+                         const idx_tensor_t* weights, const idx_tensor_t* page_table,
+                         const idx_tensor_t* row_req, const idx_tensor_t* row_start,
+                         const idx_tensor_t* row_end, const idx_tensor_t* out_scores,
+                         const idx_tensor_t* out_logits, idx_stream_t stream);
+
+/*
+ * Exact TopK of a materialised fp32 score matrix under the same total order and
+ * short-row contract (the selection half of the dense comparison path; also the
+ * entry that pins NaN / signed-zero / tie ordering on crafted matrices).
+ *   scores      f32 [R, S]   row r's candidates are scores[r, start_r .. end_r)
+ *   row_start, row_end i32 [R]
+ *   out_raw_idx i32 [R, topk]   positions (absolute within the row) or -1
+ * Requires end_r <= S (checked on the device, IDX_ERR_INVALID_METADATA).
+ */
+int idx_topk_select_scores(const idx_tensor_t* scores, const idx_tensor_t* row_start,
+                           const idx_tensor_t* row_end, int32_t topk,
+                           const idx_tensor_t* out_raw_idx, idx_stream_t stream);
+
+/*
+ * Dense comparison path: materialises fp32 scores [R, score_stride] (rows with
+ * window longer than topk), then runs the separate TopK and the page mapping.
+ * Same arguments and outputs as idx_topk_fp4_prefill plus:
+ *   score_workspace f32 [R, S_ws], S_ws >= max(row_end), caller-owned; may be
+ *                   NULL, in which case R * MP * 64 * 4 bytes are allocated
+ *                   stream-ordered for the call.
+ */
+int idx_dense_topk_fp4_prefill(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                               const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
+                               const idx_tensor_t* weights, const idx_tensor_t* page_table,
+                               const idx_tensor_t* row_req, const idx_tensor_t* row_start,
+                               const idx_tensor_t* row_end, int32_t topk,
+                               const idx_tensor_t* out_phys_slot,
+                               const idx_tensor_t* out_raw_idx,
+                               const idx_tensor_t* score_workspace, idx_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IDXTOPK_H_ */

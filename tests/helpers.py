@@ -1,0 +1,121 @@
+"""Shared helpers of the GPU tests: move a generated problem to the device, run
+the library entry points, and compare with the oracle.
+
+Comparison rules (tolerance from the method's stated bar: scores within 1e-5
+relative / 1e-6 absolute of the float64 oracle):
+  * per-head logits: exact equality (both sides are exact FP4 dot products);
+  * scores: |gpu - oracle| <= 1e-6 + 1e-5 * sum_h |w_h| * max(logit_h, 0), the
+    conditioned form of the bar (fp32 rounding of a sum that cancels can exceed
+    1e-5 of its result; it cannot exceed it relative to the sum of magnitudes);
+    every selected score additionally meets pure rtol 1e-5 / atol 1e-6;
+  * indices: the GPU's selected set must be exactly the TopK of the GPU's own
+    scores; against the oracle, differences may only involve scores within the
+    tolerance of the oracle's topk-th score, and are counted.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+RTOL = 1e-5
+ATOL = 1e-6
+
+
+def to_device(p, device="cuda"):
+    import torch
+    f = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    return dict(q_fp4=f(p.q_fp4), q_scale=f(p.q_scale), k_cache_fp4=f(p.k_cache_fp4),
+                k_scale=f(p.k_scale), weights=f(p.weights), page_table=f(p.page_table),
+                row_req=f(p.row_req), row_start=f(p.row_start), row_end=f(p.row_end))
+
+
+def run_fused(p, d=None, topk=None, raw=True, raise_on_error=True):
+    import torch
+    import fp4_sparse_attention_tma_gb300 as m
+    d = d or to_device(p)
+    K = int(topk or p.topk)
+    R = p.rows
+    phys = torch.zeros((R, K), dtype=torch.int32, device="cuda")
+    rawt = torch.zeros((R, K), dtype=torch.int32, device="cuda") if raw else None
+    code = m.idx_topk_fp4_prefill(**d, topk=K, out_phys_slot=phys, out_raw_idx=rawt,
+                                  raise_on_error=raise_on_error)
+    torch.cuda.synchronize()
+    return code, phys.cpu().numpy(), (rawt.cpu().numpy() if raw else None)
+
+
+def run_dense(p, d=None, workspace=True):
+    import torch
+    import fp4_sparse_attention_tma_gb300 as m
+    d = d or to_device(p)
+    K, R = p.topk, p.rows
+    phys = torch.zeros((R, K), dtype=torch.int32, device="cuda")
+    rawt = torch.zeros((R, K), dtype=torch.int32, device="cuda")
+    ws = torch.empty((R, max(1, p.max_end())), dtype=torch.float32, device="cuda") if workspace else None
+    m.idx_dense_topk_fp4_prefill(**d, topk=K, out_phys_slot=phys, out_raw_idx=rawt,
+                                 score_workspace=ws)
+    torch.cuda.synchronize()
+    return phys.cpu().numpy(), rawt.cpu().numpy()
+
+
+def run_debug(p, d=None, logits=False, rows=None):
+    """GPU scores [R, S] (NaN outside windows) and optionally logits [R, 64, S]."""
+    import torch
+    import fp4_sparse_attention_tma_gb300 as m
+    d = d or to_device(p)
+    S = max(1, p.max_end())
+    sc = torch.full((p.rows, S), float("nan"), dtype=torch.float32, device="cuda")
+    lg = torch.full((p.rows, 64, S), float("nan"), dtype=torch.float32, device="cuda") if logits else None
+    m.idx_fp4_debug_scores(**d, out_scores=sc, out_logits=lg)
+    torch.cuda.synchronize()
+    return sc, lg
+
+
+def score_bound(logits: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """1e-6 + 1e-5 * sum_h |w_h| * max(logit_h, 0) per slot; logits [n, 64]."""
+    return ATOL + RTOL * (np.maximum(logits, 0.0) @ np.abs(w.astype(np.float64)))
+
+
+def brute_topk(scores: np.ndarray, k: int, base: int) -> np.ndarray:
+    """Exact TopK under the total order of a float32/64 vector (for property checks)."""
+    s = np.asarray(scores, dtype=np.float64)
+    idx = np.arange(s.size)
+    nan = np.isnan(s)
+    val = np.where(nan, 0.0, s)
+    neg_zero = (val == 0) & np.signbit(val)
+    order = np.lexsort((idx, neg_zero, -val, nan))
+    out = np.full(k, -1, dtype=np.int64)
+    m = min(k, s.size)
+    out[:m] = order[:m] + base
+    return out
+
+
+def compare_rows(p, rows, g_raw, g_phys, o_raw, o_phys, o_scores_by_row):
+    """Compare GPU and oracle outputs of the listed rows.
+
+    Returns the number of set differences; asserts that each difference lies at
+    the selection boundary (oracle score within tolerance of the oracle's
+    topk-th score) and that the physical slots match the raw positions.
+    """
+    n_diff = 0
+    K = p.topk
+    for i, r in enumerate(rows):
+        req = int(p.row_req[r])
+        s0, s1 = int(p.row_start[r]), int(p.row_end[r])
+        gr, orr = g_raw[i], o_raw[i]
+        m = gr >= 0
+        assert np.array_equal(g_phys[i][m], p.page_table[req, gr[m] // 64] * 64 + gr[m] % 64), r
+        assert np.all(g_phys[i][~m] == -1)
+        if s1 - s0 <= K:
+            assert np.array_equal(gr, orr), r
+            continue
+        assert m.all(), r
+        if np.array_equal(gr, orr):
+            continue
+        sg, so = set(gr.tolist()), set(orr.tolist())
+        diff = sg ^ so
+        sc = o_scores_by_row[r]
+        kth = sc[orr[-1] - s0]
+        for idx in diff:
+            v = sc[idx - s0]
+            assert abs(v - kth) <= ATOL + RTOL * abs(kth) + 1e-7 * abs(kth), (r, idx, v, kth)
+        n_diff += len(diff) // 2
+    return n_diff
