@@ -22,9 +22,10 @@ constexpr int kDimBytes = 64;       // D / 2
 constexpr int kNumSF = 4;           // D / 32 UE8M0 scales per row
 constexpr int kPage = 64;           // slots per KV page
 constexpr int kTile = 128;          // slots per K tile = MMA M
-constexpr int kRowsPerBlock = 6;    // query rows sharing one K tile
-constexpr int kRowsPerChunk = 2;    // rows per TMEM accumulator (N = 2 * 64)
+constexpr int kRowsPerBlock = 3;    // query rows sharing one K tile (one per epilogue warpgroup)
+constexpr int kRowsPerChunk = 1;    // rows per TMEM accumulator (N = 64 heads)
 constexpr int kChunks = kRowsPerBlock / kRowsPerChunk;
+constexpr int kAccStages = 2;       // TMEM accumulators per row (double buffer)
 constexpr int kMinUnitTiles = 32;   // shortest work unit (tiles), except whole short blocks
 constexpr int kUnitsPerCta = 4;     // target work units per persistent CTA
 
@@ -143,6 +144,7 @@ struct ScoreParams {
   int64_t dense_stride;
   float* logits_out;       // [rows, 64, logits_stride] or null
   int64_t logits_stride;
+  unsigned long long* prof;  // optional [32] wait-cycle counters (by wait site % 32)
 };
 
 // Parameters of the row finishing kernels (merge of unit candidates, or TopK of

@@ -1,25 +1,27 @@
 // Fused FP4 paged-MQA scorer for sm_103a (one persistent CTA per SM).
 //
-// Per work unit (a block of up to 6 rows of one request x a run of 128-slot K
+// Per work unit (a block of up to 3 rows of one request x a run of 128-slot K
 // tiles; see idx_internal.h) the CTA
 //   * stages each K tile (2 pages of 64 slots x 64 B of E2M1 codes, plus their
 //     UE8M0 scales) with TMA, the page looked up in the page table, and the
-//     query block (6 rows x 64 heads x 64 B + scales + weights) once per unit;
+//     query block (3 rows x 64 heads x 64 B + scales + weights) once per unit;
 //   * runs the contraction logit[s, (r,h)] = sum_d k[s,d] q[r,h,d] on the
 //     tcgen05 block-scaled FP4 MMA (kind::mxf4, scale vector 32, M = 128 slots,
-//     N = 2 rows x 64 heads, K = 64 per instruction) into TMEM accumulators;
-//   * drains TMEM in three epilogue warpgroups (one per accumulator, two rows
-//     each): score[r, s] = sum_h w[r,h] * max(logit, 0) in fp32, then either
-//     streams the (score, slot) keys through the bounded shared-memory TopK
-//     (select mode) or writes the fp32 scores (dense / debug mode).
+//     N = 3 rows x 64 heads = 192, K = 64 per instruction, two per tile) into a
+//     double-buffered TMEM accumulator;
+//   * drains TMEM in three epilogue warpgroups, one per row, each holding its
+//     row's 64 weights in registers: score[r, s] = sum_h w[r,h] * max(logit, 0)
+//     in fp32, then either streams the (score, slot) keys through the bounded
+//     shared-memory TopK (select mode) or writes the fp32 scores (dense mode).
 // This realises the fused scorer + CTA-local exact TopK of "[FlyDSL] Add FP4
 // LiteTopK prefill operator" (ROCm/aiter#5309, Implementation) and
 // "[FlyDSL][DSv4] Prototype FP4 MQA streaming TopK" (ROCm/aiter#5282, Changes
 // and Scope), re-designed around TMA, tcgen05 and TMEM.
 //
 // Warp roles (512 threads): warp 0 TMA producer, warp 1 TMEM allocator + MMA
-// issuer (+ rearranges scale factors into the TMEM copy layout), warps 4..15
-// epilogue (warpgroup g = accumulator g; warp w reads TMEM lanes 32*(w%4)...).
+// issuer (one thread), warp 2 rearranges the query block's and each K tile's
+// scale factors into the TMEM copy layout, warps 4..15 epilogue (warpgroup g = row g of the block; warp w reads
+// TMEM lanes 32*(w%4) .. 32*(w%4)+31, i.e. slots of the tile).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -33,50 +35,71 @@ namespace idxk {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kStages = 4;
+constexpr int kStages = 12;      // K-tile ring (TMA latency x tile rate)
 constexpr int kEpiWarp0 = 4;
 constexpr int kEpiThreads = 128;  // one warpgroup
 
-constexpr uint32_t kPageBytes = kPage * kDimBytes;                        // 4096
-constexpr uint32_t kPageSfBytes = kPage * kNumSF;                         // 256
-constexpr uint32_t kABytes = kTile * kDimBytes;                           // 8192
-constexpr uint32_t kChunkBBytes = kRowsPerChunk * kHeads * kDimBytes;     // 8192
-constexpr uint32_t kBBytes = kChunks * kChunkBBytes;                      // 24576
-constexpr uint32_t kRowSfBytes = kHeads * kNumSF;                         // 256
-constexpr uint32_t kBlockSfBytes = kRowsPerBlock * kRowSfBytes;           // 1536
-constexpr uint32_t kBlockWBytes = kRowsPerBlock * kHeads * 4;             // 1536
+constexpr uint32_t kPageBytes = kPage * kDimBytes;                 // 4096
+constexpr uint32_t kPageSfBytes = kPage * kNumSF;                  // 256
+constexpr uint32_t kABytes = kTile * kDimBytes;                    // 8192
+constexpr uint32_t kRowBBytes = kHeads * kDimBytes;                // 4096 (one query row)
+constexpr uint32_t kBBytes = kRowsPerBlock * kRowBBytes;           // 12288
+constexpr uint32_t kRowSfBytes = kHeads * kNumSF;                  // 256
+constexpr uint32_t kSfbAtoms = (kRowsPerBlock * kHeads + 127) / 128;  // 2 atoms of 128 rows
+constexpr uint32_t kSfbAtomBytes = kSfbAtoms * 512;                // 1024
+constexpr uint32_t kBlockWBytes = kRowsPerBlock * kHeads * 4;      // 768
 
 constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + kStages * kABytes;
 constexpr uint32_t kOffSfaRaw = kOffB + 2 * kBBytes;
 constexpr uint32_t kOffSfaAtom = kOffSfaRaw + kStages * 512;
 constexpr uint32_t kOffSfbRaw = kOffSfaAtom + kStages * 512;
-constexpr uint32_t kOffSfbAtom = kOffSfbRaw + 2 * kBlockSfBytes;
-constexpr uint32_t kOffW = kOffSfbAtom + 2 * kBlockSfBytes;
+constexpr uint32_t kOffSfbAtom = kOffSfbRaw + 2 * kSfbAtomBytes;   // raw region padded to atoms
+constexpr uint32_t kOffW = kOffSfbAtom + 2 * kSfbAtomBytes;
 constexpr uint32_t kOffBar = kOffW + 2 * kBlockWBytes;
-constexpr uint32_t kOffMisc = kOffBar + 256;
+constexpr uint32_t kOffMisc = kOffBar + 512;
 constexpr uint32_t kOffHist = kOffMisc + 256;
-constexpr uint32_t kOffCand = kOffHist + kChunks * 256 * 4;
-static_assert(kOffB % 1024 == 0 && kOffA % 1024 == 0, "operand buffers must be 1 KB aligned");
-static_assert(kOffCand % 16 == 0, "candidate buffer alignment");
+constexpr uint32_t kOffProf = kOffHist + kChunks * 256 * 4;   // 32 x u64 wait counters
+constexpr uint32_t kOffCand = kOffProf + 256;
+static_assert(kOffB % 1024 == 0 && kOffA % 1024 == 0 && kRowBBytes % 1024 == 0,
+              "operand buffers must be 1 KB aligned");
+static_assert(kOffSfaAtom % 128 == 0 && kOffSfbAtom % 128 == 0 && kOffCand % 16 == 0,
+              "alignment");
 
 // misc region
-constexpr uint32_t kMiscTmem = 0, kMiscAbort = 4, kMiscCnt = 8, kMiscTau = 32, kMiscBc = 80;
+constexpr uint32_t kMiscTmem = 0, kMiscAbort = 4, kMiscCnt = 8, kMiscTau = 32, kMiscBc = 64;
 
 // barriers (8 bytes each)
-constexpr int kBarFull = 0, kBarEmpty = 4, kBarAccFull = 8, kBarAccEmpty = 11, kBarQFull = 14,
-              kBarQEmpty = 16, kBarEpiDone = 18, kBarMmaFinal = 20;
+constexpr int kBarFull = 0;                                  // [kStages]
+constexpr int kBarEmpty = kBarFull + kStages;                // [kStages]
+constexpr int kBarSfReady = kBarEmpty + kStages;             // [kStages]
+constexpr int kBarAccFull = kBarSfReady + kStages;           // [kAccStages]
+constexpr int kBarAccEmpty = kBarAccFull + kAccStages;       // [kAccStages]
+constexpr int kBarSfbReady = kBarAccEmpty + kAccStages;      // [2]
+constexpr int kBarQFull = kBarSfbReady + 2;                  // [2]
+constexpr int kBarQEmpty = kBarQFull + 2;                    // [2]
+constexpr int kBarEpiDone = kBarQEmpty + 2;                  // [2]
+constexpr int kBarMmaFinal = kBarEpiDone + 2;
+static_assert((kBarMmaFinal + 1) * 8 <= 512, "barrier region");
+
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColAcc = 0;      // + 128 * chunk
-constexpr uint32_t kColSfa = 384;    // + 4 * stage
-constexpr uint32_t kColSfb = 400;    // + 12 * q-buffer + 4 * chunk
+constexpr uint32_t kAccCols = kRowsPerBlock * kHeads;  // 192: one accumulator buffer
+constexpr uint32_t kColAcc = 0;                      // + kAccCols * stage + 64 * row
+constexpr uint32_t kColSfa = kAccStages * kAccCols;  // 384: + 4 * K stage
+constexpr uint32_t kColSfb = kColSfa + 4 * kStages;  // + 4 * kSfbAtoms * q-buffer (+ 2 * row)
+static_assert(kColSfb + 2 * 4 * kSfbAtoms <= kTmemCols, "TMEM budget");
 
-constexpr uint32_t kIdescK0 = idesc_mxf4(128, kRowsPerChunk * kHeads, 0);
-constexpr uint32_t kIdescK1 = idesc_mxf4(128, kRowsPerChunk * kHeads, 2);
+constexpr uint32_t kIdescK0 = idesc_mxf4(128, kAccCols, 0);
+constexpr uint32_t kIdescK1 = idesc_mxf4(128, kAccCols, 2);
 
-__host__ __device__ constexpr uint32_t cand_cap(int topk) { return topk > 0 ? 2u * (uint32_t)topk : 0u; }
+// Per-row candidate buffer (keys); compaction is checked every kCheckTiles
+// tiles, each adding at most 128 keys per row, so the buffer keeps
+// kCheckTiles*128 free entries above topk.
+constexpr int kCheckTiles = 4;
+__host__ __device__ constexpr uint32_t cand_cap(int topk) { return topk > 0 ? 2048u : 0u; }
+static_assert(1024 + kCheckTiles * 128 <= 2048, "candidate buffer too small for topk 1024");
 
 __host__ __device__ constexpr size_t smem_bytes_for(int mode, int topk) {
   return 1024 + kOffCand +
@@ -91,29 +114,65 @@ __device__ void mbar_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-// score = sum over heads of w * max(logit, 0); heads split over two packed
-// fp32 accumulators (even/odd pairs), summed at the end.  The fused and the
-// dense paths share this function, so their scores are bit-identical.
-__device__ __forceinline__ float head_sum(const uint32_t (&xa)[32], const uint32_t (&xb)[32],
-                                          const float* w) {
-  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+// score = sum over heads of w * max(logit, 0) in fp32.
+//
+// The ReLU of two thirds of the head pairs runs on the ALU pipe (max with 0);
+// the other third runs on the FMA pipe as x + |x| = 2 * max(x, 0), which is
+// exact.  Those pairs accumulate separately and are halved at the end: scaling
+// by two commutes with every fp32 product and sum, so the result is
+// bit-identical to applying max(x, 0) everywhere with the same summation
+// order.  Four packed accumulators keep the dependency chains short.  The
+// fused and the dense paths share this code, so their scores are identical.
+__device__ __forceinline__ constexpr bool pair_on_fma_pipe(int p) { return (p % 3) == 2; }
+
+// One head pair: acc += (relu(x0), relu(x1)) * (w0, w1), packed.  Written in
+// PTX so that the pair is formed in place from the TMEM-load registers.
+__device__ __forceinline__ void pair_fmnmx(uint64_t& acc, uint32_t x0, uint32_t x1, uint64_t w) {
+  asm("{\n\t.reg .f32 a, b;\n\t.reg .b64 v;\n\t"
+      "max.f32 a, %1, 0f00000000;\n\t"
+      "max.f32 b, %2, 0f00000000;\n\t"
+      "mov.b64 v, {a, b};\n\t"
+      "fma.rn.f32x2 %0, v, %3, %0;\n\t}"
+      : "+l"(acc)
+      : "f"(__uint_as_float(x0)), "f"(__uint_as_float(x1)), "l"(w));
+}
+
+// Same with x + |x| = 2 relu(x) on the FMA pipe (accumulated separately).
+__device__ __forceinline__ void pair_fadd(uint64_t& acc, uint32_t x0, uint32_t x1, uint64_t w) {
+  asm("{\n\t.reg .f32 a, b, c, d;\n\t.reg .b64 v;\n\t"
+      "abs.f32 c, %1;\n\t"
+      "abs.f32 d, %2;\n\t"
+      "add.f32 a, %1, c;\n\t"
+      "add.f32 b, %2, d;\n\t"
+      "mov.b64 v, {a, b};\n\t"
+      "fma.rn.f32x2 %0, v, %3, %0;\n\t}"
+      : "+l"(acc)
+      : "f"(__uint_as_float(x0)), "f"(__uint_as_float(x1)), "l"(w));
+}
+
+template <int P0>
+__device__ __forceinline__ void head_sum_part(const uint32_t (&x)[16], const uint64_t (&w2)[32],
+                                              uint64_t (&acc)[4]) {
 #pragma unroll
-  for (int h = 0; h < 32; h += 4) {
-    const float4 wv = *reinterpret_cast<const float4*>(w + h);
-    const float2 a = make_float2(fmaxf(__uint_as_float(xa[h]), 0.f), fmaxf(__uint_as_float(xa[h + 1]), 0.f));
-    const float2 b = make_float2(fmaxf(__uint_as_float(xa[h + 2]), 0.f), fmaxf(__uint_as_float(xa[h + 3]), 0.f));
-    acc0 = __ffma2_rn(a, make_float2(wv.x, wv.y), acc0);
-    acc1 = __ffma2_rn(b, make_float2(wv.z, wv.w), acc1);
+  for (int i = 0; i < 8; ++i) {
+    const int p = P0 + i;  // head pair (2p, 2p+1)
+    if (pair_on_fma_pipe(p))
+      pair_fadd(acc[2 + (i & 1)], x[2 * i], x[2 * i + 1], w2[p]);
+    else
+      pair_fmnmx(acc[i & 1], x[2 * i], x[2 * i + 1], w2[p]);
   }
-#pragma unroll
-  for (int h = 0; h < 32; h += 4) {
-    const float4 wv = *reinterpret_cast<const float4*>(w + 32 + h);
-    const float2 a = make_float2(fmaxf(__uint_as_float(xb[h]), 0.f), fmaxf(__uint_as_float(xb[h + 1]), 0.f));
-    const float2 b = make_float2(fmaxf(__uint_as_float(xb[h + 2]), 0.f), fmaxf(__uint_as_float(xb[h + 3]), 0.f));
-    acc0 = __ffma2_rn(a, make_float2(wv.x, wv.y), acc0);
-    acc1 = __ffma2_rn(b, make_float2(wv.z, wv.w), acc1);
-  }
-  return (acc0.x + acc0.y) + (acc1.x + acc1.y);
+}
+
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+  return make_float2(__uint_as_float((uint32_t)v), __uint_as_float((uint32_t)(v >> 32)));
+}
+
+__device__ __forceinline__ float head_sum_final(const uint64_t (&acc)[4]) {
+  const float2 a0 = unpack2(acc[0]), a1 = unpack2(acc[1]), b0 = unpack2(acc[2]),
+               b1 = unpack2(acc[3]);
+  const float a = (a0.x + a0.y) + (a1.x + a1.y);
+  const float b = (b0.x + b0.y) + (b1.x + b1.y);
+  return a + 0.5f * b;
 }
 
 struct UnitView {
@@ -148,14 +207,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kBarFull + s), 1);
       mbar_init(bar(kBarEmpty + s), 1);
+      mbar_init(bar(kBarSfReady + s), 1);
     }
-    for (int c = 0; c < kChunks; ++c) {
+    for (int c = 0; c < kAccStages; ++c) {
       mbar_init(bar(kBarAccFull + c), 1);
-      mbar_init(bar(kBarAccEmpty + c), 4);
+      mbar_init(bar(kBarAccEmpty + c), kRowsPerBlock * kEpiThreads);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(kBarQFull + b), 1);
       mbar_init(bar(kBarQEmpty + b), 1);
+      mbar_init(bar(kBarSfbReady + b), 1);
       mbar_init(bar(kBarEpiDone + b), (kThreads / 32) - kEpiWarp0);
     }
     mbar_init(bar(kBarMmaFinal), 1);
@@ -170,6 +231,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Optional wait profile (measurement support): cycles each warp spends in
+  // every barrier-wait site, summed per CTA in shared memory, then globally.
+  unsigned long long* prof_s = reinterpret_cast<unsigned long long*>(smem + kOffProf);
+  if (p.prof && threadIdx.x < 32) prof_s[threadIdx.x] = 0ull;
+  __syncthreads();
+  auto wait = [&](uint32_t b, uint32_t par, uint32_t site) -> bool {
+    if (!p.prof) return mbar_wait(b, par, abort_flag, hdr, site);
+    const long long c0 = clock64();
+    const bool r = mbar_wait(b, par, abort_flag, hdr, site);
+    if ((threadIdx.x & 31) == 0) atomicAdd(&prof_s[site & 31], (unsigned long long)(clock64() - c0));
+    return r;
+  };
+  auto prof_add = [&](int slot, long long c0) {
+    if (p.prof && (threadIdx.x & 31) == 0)
+      atomicAdd(&prof_s[slot], (unsigned long long)(clock64() - c0));
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer ----
@@ -178,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmap_q);
     }
     uint32_t stage = 0, sphase = 0;
-    uint32_t k_issued[kStages] = {0, 0, 0, 0};
+    uint32_t n_issued = 0;  // K tiles issued (stage s holds issues s, s+kStages, ...)
     uint32_t q_issued[2] = {0, 0};
     bool ok = true;
     for (int i = 0; ok; ++i) {
@@ -196,39 +273,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t act_mask = __ballot_sync(0xffffffffu, act);
       if (i >= 2) {
-        ok = mbar_wait(bar(kBarQEmpty + qb), qpar ^ 1u, abort_flag, hdr, 300) &&
-             mbar_wait(bar(kBarEpiDone + qb), qpar ^ 1u, abort_flag, hdr, 301);
+        ok = wait(bar(kBarQEmpty + qb), qpar ^ 1u, 300) &&
+             wait(bar(kBarEpiDone + qb), qpar ^ 1u, 301);
         if (!ok) break;
       }
       if (lane == 0) {
         uint32_t bytes = 2u * (uint32_t)uv.b.nrows * kRowSfBytes;
         for (int c = 0; c < kChunks; ++c)
-          if ((act_mask >> (2 * c)) & 3u) bytes += kChunkBBytes;
+          if ((act_mask >> c) & 1u) bytes += kRowBBytes;
         const uint32_t qf = bar(kBarQFull + qb);
         mbar_arrive_expect_tx(qf, bytes);
         for (int c = 0; c < kChunks; ++c)
-          if ((act_mask >> (2 * c)) & 3u)
-            tma_load_2d(sbase + kOffB + qb * kBBytes + c * kChunkBBytes, &tmap_q, 0,
-                        (uv.b.row0 + kRowsPerChunk * c) * kHeads, qf);
-        bulk_load(sbase + kOffSfbRaw + qb * kBlockSfBytes,
+          if ((act_mask >> c) & 1u)
+            tma_load_2d(sbase + kOffB + qb * kBBytes + c * kRowBBytes, &tmap_q, 0,
+                        (uv.b.row0 + c) * kHeads, qf);
+        bulk_load(sbase + kOffSfbRaw + qb * kSfbAtomBytes,
                   p.q_scale + (int64_t)uv.b.row0 * kRowSfBytes, uv.b.nrows * kRowSfBytes, qf);
         bulk_load(sbase + kOffW + qb * kBlockWBytes, p.weights + (int64_t)uv.b.row0 * kHeads,
                   uv.b.nrows * kHeads * 4u, qf);
       }
       ++q_issued[qb];
       const int32_t* row_pt = p.page_table + (int64_t)uv.b.req * p.max_pages;
+      // row windows of the block, broadcast to every lane
+      int32_t ws[kRowsPerBlock], we[kRowsPerBlock];
+#pragma unroll
+      for (int j = 0; j < kRowsPerBlock; ++j) {
+        const bool aj = __shfl_sync(0xffffffffu, act, j);
+        ws[j] = aj ? __shfl_sync(0xffffffffu, rs, j) : 0;
+        we[j] = aj ? __shfl_sync(0xffffffffu, re, j) : 0;
+      }
+      // page-table entries of 32 consecutive logical pages, one per lane,
+      // read only for pages that some row's window touches
+      int32_t pt_base = -64, pt_val = -1;
+      uint32_t pt_need = 0;
       for (int t = uv.u.t_begin; t < uv.u.t_end; ++t) {
-        if (!mbar_wait(bar(kBarEmpty + stage), sphase ^ 1u, abort_flag, hdr, 302)) {
+        const int32_t lp0 = 2 * t, lp1 = 2 * t + 1;
+        if (lp1 >= pt_base + 32) {
+          pt_base = lp0;
+          const int32_t lp = pt_base + lane;
+          bool need = false;
+#pragma unroll
+          for (int j = 0; j < kRowsPerBlock; ++j)
+            need |= ws[j] < (lp + 1) * kPage && we[j] > lp * kPage;
+          pt_need = __ballot_sync(0xffffffffu, need);
+          pt_val = need ? row_pt[lp] : -1;
+        }
+        const bool need0 = (pt_need >> (lp0 - pt_base)) & 1u;
+        const bool need1 = (pt_need >> (lp1 - pt_base)) & 1u;
+        const int32_t e0v = __shfl_sync(0xffffffffu, pt_val, lp0 - pt_base);
+        const int32_t e1v = __shfl_sync(0xffffffffu, pt_val, lp1 - pt_base);
+        if (!wait(bar(kBarEmpty + stage), sphase ^ 1u, 302)) {
           ok = false;
           break;
         }
-        const int32_t lp0 = 2 * t, lp1 = 2 * t + 1;
-        const bool need0 = __any_sync(0xffffffffu, act && rs < (lp0 + 1) * kPage && re > lp0 * kPage);
-        const bool need1 = __any_sync(0xffffffffu, act && rs < (lp1 + 1) * kPage && re > lp1 * kPage);
         if (lane == 0) {
           const uint32_t fb = bar(kBarFull + stage);
-          const int32_t pg0 = need0 ? row_pt[lp0] : -1;
-          const int32_t pg1 = need1 ? row_pt[lp1] : -1;
+          const int32_t pg0 = need0 ? e0v : -1;
+          const int32_t pg1 = need1 ? e1v : -1;
           const bool v0 = need0 && pg0 >= 0 && pg0 < p.num_pages;
           const bool v1 = need1 && pg1 >= 0 && pg1 < p.num_pages;
           if ((need0 && !v0) || (need1 && !v1)) raise_status(hdr, kErrInvalidPage, 303);
@@ -249,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(fb);
           }
         }
-        ++k_issued[stage];
+        ++n_issued;
         if (++stage == kStages) {
           stage = 0;
           sphase ^= 1u;
@@ -257,121 +358,129 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (lane == 0) {
-      for (int s = 0; s < kStages; ++s)
-        if (k_issued[s]) mbar_drain(bar(kBarFull + s), (k_issued[s] - 1u) & 1u);
+      for (uint32_t s = 0; s < (uint32_t)kStages; ++s) {
+        const uint32_t uses = n_issued > s ? (n_issued - s + kStages - 1) / kStages : 0;
+        if (uses) mbar_drain(bar(kBarFull + s), (uses - 1u) & 1u);
+      }
       for (int b = 0; b < 2; ++b)
         if (q_issued[b]) mbar_drain(bar(kBarQFull + b), (q_issued[b] - 1u) & 1u);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer ----
+    // One thread issues every tcgen05 operation (scale copies, MMAs,
+    // commits); descriptors and TMEM addresses advance arithmetically.
+    if (lane == 0) {
+      uint32_t stage = 0, sphase = 0, acc_use = 0;
+      const uint64_t a_desc0 = desc_kmajor_sw64(sbase + kOffA);
+      const uint64_t b_desc0 = desc_kmajor_sw64(sbase + kOffB);
+      bool ok = true;
+      for (int i = 0; ok; ++i) {
+        const int ui = blockIdx.x + i * gridDim.x;
+        if (ui >= n_units) break;
+        const UnitInfo u = p.units[p.sched[ui]];
+        const int qb = i & 1;
+        const uint32_t qpar = (uint32_t)(i >> 1) & 1u;
+        // query block landed and its scales rearranged (warp 2)
+        if (!wait(bar(kBarSfbReady + qb), qpar, 310)) break;
+        tc_fence_after();
+        const uint32_t sfb = tmem + kColSfb + 4u * kSfbAtoms * qb;
+        for (uint32_t a = 0; a < kSfbAtoms; ++a)
+          tc_cp_sf(sfb + 4u * a, desc_sf_block(sbase + kOffSfbAtom + qb * kSfbAtomBytes + 512u * a));
+        const uint64_t bd = b_desc0 + ((qb * kBBytes) >> 4);
+        for (int t = u.t_begin; t < u.t_end; ++t) {
+          // K tile landed and its scales rearranged (warp 2)
+          if (!wait(bar(kBarSfReady + stage), sphase, 312)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa = tmem + kColSfa + 4u * stage;
+          tc_cp_sf(sfa, desc_sf_block(sbase + kOffSfaAtom + stage * 512u));
+          const uint32_t b = acc_use & 1u;
+          if (!wait(bar(kBarAccEmpty + b), ((acc_use >> 1) & 1u) ^ 1u, 313)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // all rows of the block in one N = 192 instruction per K step; the
+          // second K = 64 step advances both operands by 32 bytes
+          const uint64_t ad = a_desc0 + ((stage * kABytes) >> 4);
+          const uint32_t d = tmem + kColAcc + kAccCols * b;
+          tc_mma_mxf4(d, ad, bd, kIdescK0, sfa, sfb, 0u);
+          tc_mma_mxf4(d, ad + 2, bd + 2, kIdescK1, sfa, sfb, 1u);
+          tc_commit(bar(kBarAccFull + b));
+          tc_commit(bar(kBarEmpty + stage));
+          ++acc_use;
+          if (++stage == kStages) {
+            stage = 0;
+            sphase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(bar(kBarQEmpty + qb));
+      }
+      tc_commit(bar(kBarMmaFinal));
+      mbar_drain(bar(kBarMmaFinal), 0);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------ scale-factor transposer ----
+    // Rearranges UE8M0 scales into the 32x16-byte TMEM copy layout (operand
+    // row n of a 128-row atom -> 32-bit word 4*(n%32) + n/32): the query
+    // block's scales once per unit, each K tile's scales once per tile.
     uint32_t stage = 0, sphase = 0;
-    uint32_t acc_use[kChunks] = {0, 0, 0};
     bool ok = true;
     for (int i = 0; ok; ++i) {
       const int ui = blockIdx.x + i * gridDim.x;
       if (ui >= n_units) break;
-      const UnitView uv = load_unit(p, ui);
+      const UnitInfo u = p.units[p.sched[ui]];
       const int qb = i & 1;
       const uint32_t qpar = (uint32_t)(i >> 1) & 1u;
-      bool act = false;
-      if (lane < uv.b.nrows) {
-        const int32_t rs = p.row_start[uv.b.row0 + lane], re = p.row_end[uv.b.row0 + lane];
-        act = (re - rs) > p.score_thr;
-      }
-      const uint32_t act_mask = __ballot_sync(0xffffffffu, act);
-      uint32_t cmask = 0;
-      for (int c = 0; c < kChunks; ++c)
-        if ((act_mask >> (2 * c)) & 3u) cmask |= 1u << c;
-      if (!mbar_wait(bar(kBarQFull + qb), qpar, abort_flag, hdr, 310)) break;
-      if (i >= 2 && !mbar_wait(bar(kBarQEmpty + qb), qpar ^ 1u, abort_flag, hdr, 311)) break;
+      if (!wait(bar(kBarQFull + qb), qpar, 331)) break;
+      // the MMA thread's copy of this buffer two units ago has completed
+      if (i >= 2 && !wait(bar(kBarQEmpty + qb), qpar ^ 1u, 332)) break;
       {
-        // query scales [row][head][4] -> per chunk of 128 (row, head) rows, the
-        // 32x16-byte TMEM copy layout: row n -> word 4*(n%32) + n/32
-        const uint32_t* raw = reinterpret_cast<const uint32_t*>(smem + kOffSfbRaw + qb * kBlockSfBytes);
-        uint32_t* atom = reinterpret_cast<uint32_t*>(smem + kOffSfbAtom + qb * kBlockSfBytes);
-        for (int idx = lane; idx < kChunks * 128; idx += 32) {
-          const int c = idx >> 7, n = idx & 127;
-          atom[c * 128 + 4 * (n & 31) + (n >> 5)] = raw[idx];
+        const uint32_t* raw = reinterpret_cast<const uint32_t*>(smem + kOffSfbRaw + qb * kSfbAtomBytes);
+        uint32_t* atom = reinterpret_cast<uint32_t*>(smem + kOffSfbAtom + qb * kSfbAtomBytes);
+#pragma unroll
+        for (int k = 0; k < (int)kSfbAtoms * 4; ++k) {
+          const int a = k >> 2, j = k & 3;  // atom, 32-row group
+          atom[a * 128 + 4 * lane + j] = raw[a * 128 + 32 * j + lane];
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          tc_fence_after();
-          for (int c = 0; c < kChunks; ++c)
-            if ((cmask >> c) & 1u)
-              tc_cp_sf(tmem + kColSfb + 12u * qb + 4u * c,
-                       desc_sf_block(sbase + kOffSfbAtom + qb * kBlockSfBytes + 512u * c));
-        }
-        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarSfbReady + qb));
       }
-      for (int t = uv.u.t_begin; t < uv.u.t_end && ok; ++t) {
-        if (!mbar_wait(bar(kBarFull + stage), sphase, abort_flag, hdr, 312)) {
+      for (int t = u.t_begin; t < u.t_end; ++t) {
+        if (!wait(bar(kBarFull + stage), sphase, 330)) {
           ok = false;
           break;
         }
-        {
-          const uint32_t* raw = reinterpret_cast<const uint32_t*>(smem + kOffSfaRaw + stage * 512u);
-          uint32_t* atom = reinterpret_cast<uint32_t*>(smem + kOffSfaAtom + stage * 512u);
-          for (int idx = lane; idx < 128; idx += 32) atom[4 * (idx & 31) + (idx >> 5)] = raw[idx];
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tc_fence_after();
-            tc_cp_sf(tmem + kColSfa + 4u * stage, desc_sf_block(sbase + kOffSfaAtom + stage * 512u));
-          }
-          __syncwarp();
-        }
+        const uint32_t* raw = reinterpret_cast<const uint32_t*>(smem + kOffSfaRaw + stage * 512u);
+        uint32_t* atom = reinterpret_cast<uint32_t*>(smem + kOffSfaAtom + stage * 512u);
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c) {
-          if (!((cmask >> c) & 1u)) continue;
-          if (!mbar_wait(bar(kBarAccEmpty + c), (acc_use[c] & 1u) ^ 1u, abort_flag, hdr, 313)) {
-            ok = false;
-            break;
-          }
-          if (lane == 0) {
-            tc_fence_after();
-            const uint64_t ad = desc_kmajor_sw64(sbase + kOffA + stage * kABytes);
-            const uint64_t bd = desc_kmajor_sw64(sbase + kOffB + qb * kBBytes + c * kChunkBBytes);
-            const uint32_t d = tmem + kColAcc + 128u * c;
-            const uint32_t sfa = tmem + kColSfa + 4u * stage;
-            const uint32_t sfb = tmem + kColSfb + 12u * qb + 4u * c;
-            tc_mma_mxf4(d, ad, bd, kIdescK0, sfa, sfb, 0u);
-            // second K=64 step: operands advance 32 bytes along K
-            tc_mma_mxf4(d, ad + 2, bd + 2, kIdescK1, sfa, sfb, 1u);
-            tc_commit(bar(kBarAccFull + c));
-          }
-          __syncwarp();
-          ++acc_use[c];
-        }
-        if (!ok) break;
-        if (lane == 0) tc_commit(bar(kBarEmpty + stage));
+        for (int j = 0; j < 4; ++j) atom[4 * lane + j] = raw[32 * j + lane];
+        fence_proxy_async_smem();
         __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarSfReady + stage));
         if (++stage == kStages) {
           stage = 0;
           sphase ^= 1u;
         }
       }
-      if (!ok) break;
-      if (lane == 0) tc_commit(bar(kBarQEmpty + qb));
-      __syncwarp();
     }
-    if (lane == 0) {
-      tc_commit(bar(kBarMmaFinal));
-      mbar_drain(bar(kBarMmaFinal), 0);
-    }
-    __syncwarp();
   } else if (warp >= kEpiWarp0) {
     // --------------------------------------------------------- epilogue ----
-    const int g = (warp - kEpiWarp0) >> 2;  // accumulator / warpgroup
+    const int g = (warp - kEpiWarp0) >> 2;  // row of the block handled by this warpgroup
     const int qd = warp & 3;                 // TMEM lane quarter
     const int tg = qd * 32 + lane;           // slot within tile == thread in group
     const uint32_t bar_id = 1u + (uint32_t)g;
     constexpr uint32_t kCap = cand_cap(TOPK);
-    uint32_t* cnt_s = reinterpret_cast<uint32_t*>(smem + kOffMisc + kMiscCnt);
-    uint64_t* tau_s = reinterpret_cast<uint64_t*>(smem + kOffMisc + kMiscTau);
+    uint32_t* cnt_s = reinterpret_cast<uint32_t*>(smem + kOffMisc + kMiscCnt) + g;
+    uint64_t* tau_s = reinterpret_cast<uint64_t*>(smem + kOffMisc + kMiscTau) + g;
     uint32_t* bc = reinterpret_cast<uint32_t*>(smem + kOffMisc + kMiscBc) + 4 * g;
     uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kOffHist) + 256 * g;
-    uint64_t* cand = reinterpret_cast<uint64_t*>(smem + kOffCand);
+    uint64_t* cand = reinterpret_cast<uint64_t*>(smem + kOffCand) + (size_t)g * kCap;
     uint32_t acc_use = 0;
     bool ok = true;
     for (int i = 0; ok; ++i) {
@@ -380,109 +489,130 @@ __global__ void __launch_bounds__(kThreads, 1)
       const UnitView uv = load_unit(p, ui);
       const int qb = i & 1;
       const uint32_t qpar = (uint32_t)(i >> 1) & 1u;
-      int32_t s_j[2], e_j[2];
-      bool act_j[2], valid_j[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int rj = kRowsPerChunk * g + j;
-        valid_j[j] = rj < uv.b.nrows;
-        s_j[j] = valid_j[j] ? p.row_start[uv.b.row0 + rj] : 0;
-        e_j[j] = valid_j[j] ? p.row_end[uv.b.row0 + rj] : 0;
-        act_j[j] = valid_j[j] && (e_j[j] - s_j[j]) > p.score_thr;
-      }
-      if (act_j[0] || act_j[1]) {
-        if (!mbar_wait(bar(kBarQFull + qb), qpar, abort_flag, hdr, 320)) {
+      const bool valid = g < uv.b.nrows;
+      const int64_t row = uv.b.row0 + g;
+      const int32_t s0 = valid ? p.row_start[row] : 0;
+      const int32_t e0 = valid ? p.row_end[row] : 0;
+      const bool act = valid && (e0 - s0) > p.score_thr;
+      if (!act) {
+        // this row is not scored, but every warpgroup releases each
+        // accumulator buffer, so walk the unit's tiles
+        for (int t = uv.u.t_begin; t < uv.u.t_end; ++t) {
+          const uint32_t b = acc_use & 1u;
+          if (!wait(bar(kBarAccFull + b), (acc_use >> 1) & 1u, 322)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mbar_arrive(bar(kBarAccEmpty + b));
+          ++acc_use;
+        }
+        if (MODE == kModeSelect && valid && tg == 0)
+          p.cand_cnt[uv.b.slot0 + (int64_t)uv.u.k * uv.b.nrows + g] = 0;
+      } else {
+        if (!wait(bar(kBarQFull + qb), qpar, 320)) {
           ok = false;
         } else {
-          const float* wrow = reinterpret_cast<const float*>(smem + kOffW + qb * kBlockWBytes);
-          uint64_t tau[2] = {0ull, 0ull};
+          uint64_t w2[32];  // the row's weights as packed pairs (heads 2p, 2p+1)
+          const ulonglong2* wsrc =
+              reinterpret_cast<const ulonglong2*>(smem + kOffW + qb * kBlockWBytes) + g * (kHeads / 4);
+          auto load_w2 = [&]() {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const ulonglong2 v = wsrc[k];
+              w2[2 * k] = v.x;
+              w2[2 * k + 1] = v.y;
+            }
+          };
+          load_w2();
+          uint32_t thi = 0, tlo = 0;  // threshold key (score key, ~index)
+          bool over = false;
           if constexpr (MODE == kModeSelect) {
-            if (tg < 2) {
-              cnt_s[kRowsPerChunk * g + tg] = 0;
-              tau_s[kRowsPerChunk * g + tg] = 0ull;
+            if (tg == 0) {
+              *cnt_s = 0;
+              *tau_s = 0ull;
             }
             bar_sync(bar_id, kEpiThreads);
           }
+          const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16) + kColAcc + 64u * g;
           for (int t = uv.u.t_begin; t < uv.u.t_end; ++t) {
-            if (!mbar_wait(bar(kBarAccFull + g), acc_use & 1u, abort_flag, hdr, 321)) {
+            const uint32_t b = acc_use & 1u;
+            const uint32_t ph = (acc_use >> 1) & 1u;
+            if (!wait(bar(kBarAccFull + b), ph, 321)) {
               ok = false;
               break;
             }
             tc_fence_after();
+            const uint32_t tb = lane_base + kAccCols * b;
             const int32_t slot = t * kTile + tg;
-            const uint32_t tbase = tmem + ((uint32_t)(qd * 32) << 16) + kColAcc + 128u * g;
-            bool over = false;
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              if (!act_j[j]) continue;
-              const int rj = kRowsPerChunk * g + j;
-              uint32_t xa[32], xb[32];
-              tmem_ld32(tbase + 64u * j, xa);
-              tmem_ld32(tbase + 64u * j + 32u, xb);
-              tmem_wait_ld();
-              if (j == 1 || !act_j[1]) {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kBarAccEmpty + g));
-              }
-              const float sc = head_sum(xa, xb, wrow + rj * kHeads);
-              const bool in_win = slot >= s_j[j] && slot < e_j[j];
+            const bool in_win = (uint32_t)(slot - s0) < (uint32_t)(e0 - s0);
+            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // four packed (+0, +0) sums
+            // four 16-column TMEM loads, each issued before the previous
+            // chunk is reduced (a wait covers every load issued before it)
+            uint32_t xa[16], xb[16];
+            auto dump = [&](const uint32_t(&x)[16], int h0) {
               if constexpr (MODE == kModeDense) {
-                const int64_t row = uv.b.row0 + rj;
-                if (in_win) {
-                  p.dense_out[row * p.dense_stride + slot] = sc;
-                  if (p.logits_out) {
-                    float* lo = p.logits_out + row * kHeads * p.logits_stride + slot;
+                if (p.logits_out && in_win) {
+                  float* lo = p.logits_out + (row * kHeads + h0) * p.logits_stride + slot;
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) lo[(int64_t)h * p.logits_stride] = __uint_as_float(xa[h]);
-#pragma unroll
-                    for (int h = 0; h < 32; ++h)
-                      lo[(int64_t)(32 + h) * p.logits_stride] = __uint_as_float(xb[h]);
-                  }
+                  for (int h = 0; h < 16; ++h) lo[(int64_t)h * p.logits_stride] = __uint_as_float(x[h]);
                 }
-              } else {
-                const uint64_t key = order_key(sc, slot);
-                const bool pass = in_win && key >= tau[j];
-                over |= sel_append(cand + (size_t)rj * kCap, cnt_s + rj, kCap, kCap - kEpiThreads,
-                                   pass, key);
               }
-            }
+            };
+            tmem_ld16(tb, xa);
+            tmem_wait_ld16(xa);
+            tmem_ld16(tb + 16u, xb);
+            dump(xa, 0);
+            head_sum_part<0>(xa, w2, acc);
+            tmem_wait_ld16(xb);
+            tmem_ld16(tb + 32u, xa);
+            dump(xb, 16);
+            head_sum_part<8>(xb, w2, acc);
+            tmem_wait_ld16(xa);
+            tmem_ld16(tb + 48u, xb);
+            dump(xa, 32);
+            head_sum_part<16>(xa, w2, acc);
+            tmem_wait_ld16(xb);
+            tc_fence_before();
+            mbar_arrive(bar(kBarAccEmpty + b));
             ++acc_use;
-            if constexpr (MODE == kModeSelect) {
-              if (bar_red_or(bar_id, kEpiThreads, over)) {
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                  if (!act_j[j]) continue;
-                  const int rj = kRowsPerChunk * g + j;
-                  if (*(volatile uint32_t*)(cnt_s + rj) > kCap - kEpiThreads)
-                    sel_compact<kEpiThreads, kCap>(cand + (size_t)rj * kCap, cnt_s + rj, tau_s + rj,
-                                                   hist, bc, (uint32_t)TOPK, tg, bar_id, hdr);
-                  tau[j] = *(volatile uint64_t*)(tau_s + rj);
+            dump(xb, 48);
+            head_sum_part<24>(xb, w2, acc);
+            const float sc = head_sum_final(acc);
+            if constexpr (MODE == kModeDense) {
+              if (in_win) p.dense_out[row * p.dense_stride + slot] = sc;
+            } else {
+              // cheap 32-bit test first; the low word only decides exact ties
+              const uint32_t k32 = score_key(sc);
+              const bool pass = in_win & ((k32 > thi) | ((k32 == thi) & (~(uint32_t)slot >= tlo)));
+              const uint64_t key = ((uint64_t)k32 << 32) | (uint64_t)(~(uint32_t)slot);
+              over |= sel_append(cand, cnt_s, kCap, kCap - kCheckTiles * kEpiThreads, pass, key);
+              const bool check = ((t - uv.u.t_begin) % kCheckTiles) == kCheckTiles - 1;
+              if (check) {
+                if (bar_red_or(bar_id, kEpiThreads, over)) {
+                  sel_compact<kEpiThreads, kCap>(cand, cnt_s, tau_s, hist, bc, (uint32_t)TOPK, tg,
+                                                 bar_id, hdr);
+                  const uint64_t tk = *(volatile uint64_t*)tau_s;
+                  thi = (uint32_t)(tk >> 32);
+                  tlo = (uint32_t)(tk & 0xffffffffu);
+                  load_w2();  // the weights are not kept live across the compaction
                 }
+                over = false;
               }
             }
           }
           if constexpr (MODE == kModeSelect) {
-           if (ok) {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const int rj = kRowsPerChunk * g + j;
-              if (!valid_j[j]) continue;
-              const int64_t slot_idx = uv.b.slot0 + (int64_t)uv.u.k * uv.b.nrows + rj;
-              if (!act_j[j]) {
-                if (tg == 0) p.cand_cnt[slot_idx] = 0;
-                continue;
-              }
-              sel_compact<kEpiThreads, kCap>(cand + (size_t)rj * kCap, cnt_s + rj, tau_s + rj, hist,
-                                             bc, (uint32_t)TOPK, tg, bar_id, hdr);
-              const uint32_t n = min(*(volatile uint32_t*)(cnt_s + rj), (uint32_t)TOPK);
+            if (ok) {
+              const int64_t slot_idx = uv.b.slot0 + (int64_t)uv.u.k * uv.b.nrows + g;
+              bar_sync(bar_id, kEpiThreads);
+              sel_compact<kEpiThreads, kCap>(cand, cnt_s, tau_s, hist, bc, (uint32_t)TOPK, tg, bar_id,
+                                             hdr);
+              const uint32_t n = min(*(volatile uint32_t*)cnt_s, (uint32_t)TOPK);
               uint64_t* dst = p.cand_keys + slot_idx * TOPK;
-              const uint64_t* src = cand + (size_t)rj * kCap;
-              for (uint32_t e = tg; e < n; e += kEpiThreads) dst[e] = src[e];
+              for (uint32_t e = tg; e < n; e += kEpiThreads) dst[e] = cand[e];
               if (tg == 0) p.cand_cnt[slot_idx] = n;
+              bar_sync(bar_id, kEpiThreads);
             }
-            bar_sync(bar_id, kEpiThreads);
-           }
           }
         }
       }
@@ -497,6 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if (p.prof && threadIdx.x < 32) atomicAdd(&p.prof[threadIdx.x], prof_s[threadIdx.x]);
 }
 
 template <int MODE, int TOPK>
