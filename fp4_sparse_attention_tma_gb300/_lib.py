@@ -94,7 +94,6 @@ EXPORTS = {
     "idx_topk_scratch_high_water": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(ctypes.c_uint64)]),
     "idx_topk_set_timing": (ctypes.c_int, [ctypes.c_int32]),
     "idx_topk_last_timings": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float)]),
-    "idx_topk_set_wait_profile": (ctypes.c_int, [ctypes.c_void_p]),
 }
 
 

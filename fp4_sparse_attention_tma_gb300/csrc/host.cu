@@ -35,7 +35,6 @@ DeviceState g_dev[kMaxDevices];
 // Optional per-kernel timing of the last call (CUDA events on the caller's
 // stream around each launch): plan+page check, scorer, finish, whole call.
 bool g_timing = false;
-unsigned long long* g_wait_prof = nullptr;  // optional device counters of the scorer
 thread_local float g_last_ms[4] = {0.f, 0.f, 0.f, 0.f};
 
 struct CallTimer {
@@ -470,7 +469,6 @@ int run(const Call& c, cudaStream_t stream) {
   sp.dense_stride = score_stride;
   sp.logits_out = c.logits ? (float*)c.logits->data : nullptr;
   sp.logits_stride = logits_stride;
-  sp.prof = g_wait_prof;
   timer.mark(1, stream);
   cuda_err |= launch_score(tmap_k, tmap_q, sp, grid, stream) != cudaSuccess;
   timer.mark(2, stream);
@@ -645,11 +643,6 @@ int idx_topk_fp4_scratch_bytes(int32_t rows, int32_t topk, int32_t device, uint6
 
 int idx_topk_set_timing(int32_t enable) {
   g_timing = enable != 0;
-  return IDX_OK;
-}
-
-int idx_topk_set_wait_profile(void* device_counters) {
-  g_wait_prof = (unsigned long long*)device_counters;
   return IDX_OK;
 }
 

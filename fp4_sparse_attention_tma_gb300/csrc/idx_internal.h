@@ -144,7 +144,6 @@ struct ScoreParams {
   int64_t dense_stride;
   float* logits_out;       // [rows, 64, logits_stride] or null
   int64_t logits_stride;
-  unsigned long long* prof;  // optional [32] wait-cycle counters (by wait site % 32)
 };
 
 // Parameters of the row finishing kernels (merge of unit candidates, or TopK of

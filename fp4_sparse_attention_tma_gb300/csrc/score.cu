@@ -18,7 +18,7 @@
 // "[FlyDSL][DSv4] Prototype FP4 MQA streaming TopK" (ROCm/aiter#5282, Changes
 // and Scope), re-designed around TMA, tcgen05 and TMEM.
 //
-// Warp roles (512 threads): warp 0 TMA producer, warp 1 TMEM allocator + MMA
+// Warp roles (512 threads): warps 0 and 3 TMA producers (alternate K tiles), warp 1 TMEM allocator + MMA
 // issuer (one thread), warp 2 rearranges the query block's and each K tile's
 // scale factors into the TMEM copy layout, warps 4..15 epilogue (warpgroup g = row g of the block; warp w reads
 // TMEM lanes 32*(w%4) .. 32*(w%4)+31, i.e. slots of the tile).
@@ -37,6 +37,8 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kStages = 12;      // K-tile ring (TMA latency x tile rate)
 constexpr int kEpiWarp0 = 4;
+constexpr int kProducer2 = 3;  // second TMA producer warp
+static_assert(kStages % 2 == 0, "producers own the stages of one parity each");
 constexpr int kEpiThreads = 128;  // one warpgroup
 
 constexpr uint32_t kPageBytes = kPage * kDimBytes;                 // 4096
@@ -59,8 +61,7 @@ constexpr uint32_t kOffW = kOffSfbAtom + 2 * kSfbAtomBytes;
 constexpr uint32_t kOffBar = kOffW + 2 * kBlockWBytes;
 constexpr uint32_t kOffMisc = kOffBar + 512;
 constexpr uint32_t kOffHist = kOffMisc + 256;
-constexpr uint32_t kOffProf = kOffHist + kChunks * 256 * 4;   // 32 x u64 wait counters
-constexpr uint32_t kOffCand = kOffProf + 256;
+constexpr uint32_t kOffCand = kOffHist + kChunks * 256 * 4;
 static_assert(kOffB % 1024 == 0 && kOffA % 1024 == 0 && kRowBBytes % 1024 == 0,
               "operand buffers must be 1 KB aligned");
 static_assert(kOffSfaAtom % 128 == 0 && kOffSfbAtom % 128 == 0 && kOffCand % 16 == 0,
@@ -97,9 +98,9 @@ constexpr uint32_t kIdescK1 = idesc_mxf4(128, kAccCols, 2);
 // Per-row candidate buffer (keys); compaction is checked every kCheckTiles
 // tiles, each adding at most 128 keys per row, so the buffer keeps
 // kCheckTiles*128 free entries above topk.
-constexpr int kCheckTiles = 4;
-__host__ __device__ constexpr uint32_t cand_cap(int topk) { return topk > 0 ? 2048u : 0u; }
-static_assert(1024 + kCheckTiles * 128 <= 2048, "candidate buffer too small for topk 1024");
+constexpr int kCheckTiles = 8;
+__host__ __device__ constexpr uint32_t cand_cap(int topk) { return topk > 0 ? 2560u : 0u; }
+static_assert(1024 + kCheckTiles * 128 <= 2560, "candidate buffer too small for topk 1024");
 
 __host__ __device__ constexpr size_t smem_bytes_for(int mode, int topk) {
   return 1024 + kOffCand +
@@ -116,14 +117,10 @@ __device__ void mbar_drain(uint32_t bar, uint32_t parity) {
 
 // score = sum over heads of w * max(logit, 0) in fp32.
 //
-// The ReLU of two thirds of the head pairs runs on the ALU pipe (max with 0);
-// the other third runs on the FMA pipe as x + |x| = 2 * max(x, 0), which is
-// exact.  Those pairs accumulate separately and are halved at the end: scaling
-// by two commutes with every fp32 product and sum, so the result is
-// bit-identical to applying max(x, 0) everywhere with the same summation
-// order.  Four packed accumulators keep the dependency chains short.  The
-// fused and the dense paths share this code, so their scores are identical.
-__device__ __forceinline__ constexpr bool pair_on_fma_pipe(int p) { return (p % 3) == 2; }
+// Each head pair is rectified with two max-with-zero operations and folded into
+// one of four packed (f32x2) accumulators by a single paired FMA; four
+// accumulators keep the dependency chains short.  The fused and the dense
+// paths share this code, so their scores are bit-identical.
 
 // One head pair: acc += (relu(x0), relu(x1)) * (w0, w1), packed.  Written in
 // PTX so that the pair is formed in place from the TMEM-load registers.
@@ -137,29 +134,29 @@ __device__ __forceinline__ void pair_fmnmx(uint64_t& acc, uint32_t x0, uint32_t 
       : "f"(__uint_as_float(x0)), "f"(__uint_as_float(x1)), "l"(w));
 }
 
-// Same with x + |x| = 2 relu(x) on the FMA pipe (accumulated separately).
-__device__ __forceinline__ void pair_fadd(uint64_t& acc, uint32_t x0, uint32_t x1, uint64_t w) {
-  asm("{\n\t.reg .f32 a, b, c, d;\n\t.reg .b64 v;\n\t"
-      "abs.f32 c, %1;\n\t"
-      "abs.f32 d, %2;\n\t"
-      "add.f32 a, %1, c;\n\t"
-      "add.f32 b, %2, d;\n\t"
+// The first product of each accumulator: acc = (relu(x0), relu(x1)) * (w0, w1).
+__device__ __forceinline__ void pair_fmnmx_init(uint64_t& acc, uint32_t x0, uint32_t x1, uint64_t w) {
+  asm("{\n\t.reg .f32 a, b;\n\t.reg .b64 v;\n\t"
+      "max.f32 a, %1, 0f00000000;\n\t"
+      "max.f32 b, %2, 0f00000000;\n\t"
       "mov.b64 v, {a, b};\n\t"
-      "fma.rn.f32x2 %0, v, %3, %0;\n\t}"
-      : "+l"(acc)
+      "mul.rn.f32x2 %0, v, %3;\n\t}"
+      : "=l"(acc)
       : "f"(__uint_as_float(x0)), "f"(__uint_as_float(x1)), "l"(w));
 }
 
+// Heads 2*P0 .. 2*P0+15 from one 16-column TMEM load.  P0 == 0 starts the four
+// accumulators with plain products instead of adding to zero: the sums differ
+// at most in the sign of an all-zero total, which head_sum_final normalises.
 template <int P0>
 __device__ __forceinline__ void head_sum_part(const uint32_t (&x)[16], const uint64_t (&w2)[32],
                                               uint64_t (&acc)[4]) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int p = P0 + i;  // head pair (2p, 2p+1)
-    if (pair_on_fma_pipe(p))
-      pair_fadd(acc[2 + (i & 1)], x[2 * i], x[2 * i + 1], w2[p]);
+  for (int i = 0; i < 8; ++i) {  // head pair (2p, 2p+1), p = P0 + i
+    if (P0 == 0 && i < 4)
+      pair_fmnmx_init(acc[i], x[2 * i], x[2 * i + 1], w2[i]);
     else
-      pair_fmnmx(acc[i & 1], x[2 * i], x[2 * i + 1], w2[p]);
+      pair_fmnmx(acc[i & 3], x[2 * i], x[2 * i + 1], w2[P0 + i]);
   }
 }
 
@@ -170,9 +167,8 @@ __device__ __forceinline__ float2 unpack2(uint64_t v) {
 __device__ __forceinline__ float head_sum_final(const uint64_t (&acc)[4]) {
   const float2 a0 = unpack2(acc[0]), a1 = unpack2(acc[1]), b0 = unpack2(acc[2]),
                b1 = unpack2(acc[3]);
-  const float a = (a0.x + a0.y) + (a1.x + a1.y);
-  const float b = (b0.x + b0.y) + (b1.x + b1.y);
-  return a + 0.5f * b;
+  // + 0 turns an all-zero total of -0 into +0, the value a sum started at +0 has
+  return (((a0.x + a0.y) + (a1.x + a1.y)) + ((b0.x + b0.y) + (b1.x + b1.y))) + 0.0f;
 }
 
 struct UnitView {
@@ -231,31 +227,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // Optional wait profile (measurement support): cycles each warp spends in
-  // every barrier-wait site, summed per CTA in shared memory, then globally.
-  unsigned long long* prof_s = reinterpret_cast<unsigned long long*>(smem + kOffProf);
-  if (p.prof && threadIdx.x < 32) prof_s[threadIdx.x] = 0ull;
-  __syncthreads();
   auto wait = [&](uint32_t b, uint32_t par, uint32_t site) -> bool {
-    if (!p.prof) return mbar_wait(b, par, abort_flag, hdr, site);
-    const long long c0 = clock64();
-    const bool r = mbar_wait(b, par, abort_flag, hdr, site);
-    if ((threadIdx.x & 31) == 0) atomicAdd(&prof_s[site & 31], (unsigned long long)(clock64() - c0));
-    return r;
-  };
-  auto prof_add = [&](int slot, long long c0) {
-    if (p.prof && (threadIdx.x & 31) == 0)
-      atomicAdd(&prof_s[slot], (unsigned long long)(clock64() - c0));
+    return mbar_wait(b, par, abort_flag, hdr, site);
   };
 
-  if (warp == 0) {
-    // ------------------------------------------------------ TMA producer ----
-    if (lane == 0) {
+  if (warp == 0 || warp == kProducer2) {
+    // ----------------------------------------------------- TMA producers ----
+    // Two warps share the K ring: tile n of the CTA's sequence (stage
+    // n % kStages) is issued by warp 0 when n is even and by the second
+    // producer when n is odd, so two copy streams are in flight at once.  Warp
+    // 0 also loads each unit's query block.
+    const uint32_t pw = warp == 0 ? 0u : 1u;
+    if (lane == 0 && pw == 0) {
       prefetch_tmap(&tmap_k);
       prefetch_tmap(&tmap_q);
     }
     uint32_t stage = 0, sphase = 0;
-    uint32_t n_issued = 0;  // K tiles issued (stage s holds issues s, s+kStages, ...)
+    uint32_t n_issued = 0;  // K tiles of the CTA's sequence so far (both producers)
     uint32_t q_issued[2] = {0, 0};
     bool ok = true;
     for (int i = 0; ok; ++i) {
@@ -272,27 +260,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         act = (re - rs) > p.score_thr;
       }
       const uint32_t act_mask = __ballot_sync(0xffffffffu, act);
-      if (i >= 2) {
-        ok = wait(bar(kBarQEmpty + qb), qpar ^ 1u, 300) &&
-             wait(bar(kBarEpiDone + qb), qpar ^ 1u, 301);
-        if (!ok) break;
+      if (pw == 0) {
+        if (i >= 2) {
+          ok = wait(bar(kBarQEmpty + qb), qpar ^ 1u, 300) &&
+               wait(bar(kBarEpiDone + qb), qpar ^ 1u, 301);
+          if (!ok) break;
+        }
+        if (lane == 0) {
+          uint32_t bytes = 2u * (uint32_t)uv.b.nrows * kRowSfBytes;
+          for (int c = 0; c < kChunks; ++c)
+            if ((act_mask >> c) & 1u) bytes += kRowBBytes;
+          const uint32_t qf = bar(kBarQFull + qb);
+          mbar_arrive_expect_tx(qf, bytes);
+          for (int c = 0; c < kChunks; ++c)
+            if ((act_mask >> c) & 1u)
+              tma_load_2d(sbase + kOffB + qb * kBBytes + c * kRowBBytes, &tmap_q, 0,
+                          (uv.b.row0 + c) * kHeads, qf);
+          bulk_load(sbase + kOffSfbRaw + qb * kSfbAtomBytes,
+                    p.q_scale + (int64_t)uv.b.row0 * kRowSfBytes, uv.b.nrows * kRowSfBytes, qf);
+          bulk_load(sbase + kOffW + qb * kBlockWBytes, p.weights + (int64_t)uv.b.row0 * kHeads,
+                    uv.b.nrows * kHeads * 4u, qf);
+        }
+        ++q_issued[qb];
       }
-      if (lane == 0) {
-        uint32_t bytes = 2u * (uint32_t)uv.b.nrows * kRowSfBytes;
-        for (int c = 0; c < kChunks; ++c)
-          if ((act_mask >> c) & 1u) bytes += kRowBBytes;
-        const uint32_t qf = bar(kBarQFull + qb);
-        mbar_arrive_expect_tx(qf, bytes);
-        for (int c = 0; c < kChunks; ++c)
-          if ((act_mask >> c) & 1u)
-            tma_load_2d(sbase + kOffB + qb * kBBytes + c * kRowBBytes, &tmap_q, 0,
-                        (uv.b.row0 + c) * kHeads, qf);
-        bulk_load(sbase + kOffSfbRaw + qb * kSfbAtomBytes,
-                  p.q_scale + (int64_t)uv.b.row0 * kRowSfBytes, uv.b.nrows * kRowSfBytes, qf);
-        bulk_load(sbase + kOffW + qb * kBlockWBytes, p.weights + (int64_t)uv.b.row0 * kHeads,
-                  uv.b.nrows * kHeads * 4u, qf);
-      }
-      ++q_issued[qb];
       const int32_t* row_pt = p.page_table + (int64_t)uv.b.req * p.max_pages;
       // row windows of the block, broadcast to every lane
       int32_t ws[kRowsPerBlock], we[kRowsPerBlock];
@@ -307,6 +297,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       int32_t pt_base = -64, pt_val = -1;
       uint32_t pt_need = 0;
       for (int t = uv.u.t_begin; t < uv.u.t_end; ++t) {
+        const bool mine = (n_issued & 1u) == pw;
+        const uint32_t st = stage, sp = sphase;
+        ++n_issued;
+        if (++stage == kStages) {
+          stage = 0;
+          sphase ^= 1u;
+        }
+        if (!mine) continue;
         const int32_t lp0 = 2 * t, lp1 = 2 * t + 1;
         if (lp1 >= pt_base + 32) {
           pt_base = lp0;
@@ -322,12 +320,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool need1 = (pt_need >> (lp1 - pt_base)) & 1u;
         const int32_t e0v = __shfl_sync(0xffffffffu, pt_val, lp0 - pt_base);
         const int32_t e1v = __shfl_sync(0xffffffffu, pt_val, lp1 - pt_base);
-        if (!wait(bar(kBarEmpty + stage), sphase ^ 1u, 302)) {
+        if (!wait(bar(kBarEmpty + st), sp ^ 1u, 302)) {
           ok = false;
           break;
         }
         if (lane == 0) {
-          const uint32_t fb = bar(kBarFull + stage);
+          const uint32_t fb = bar(kBarFull + st);
           const int32_t pg0 = need0 ? e0v : -1;
           const int32_t pg1 = need1 ? e1v : -1;
           const bool v0 = need0 && pg0 >= 0 && pg0 < p.num_pages;
@@ -336,8 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t bytes = ((uint32_t)v0 + (uint32_t)v1) * (kPageBytes + kPageSfBytes);
           if (bytes) {
             mbar_arrive_expect_tx(fb, bytes);
-            const uint32_t a = sbase + kOffA + stage * kABytes;
-            const uint32_t sf = sbase + kOffSfaRaw + stage * 512u;
+            const uint32_t a = sbase + kOffA + st * kABytes;
+            const uint32_t sf = sbase + kOffSfaRaw + st * 512u;
             if (v0) {
               tma_load_2d(a, &tmap_k, 0, pg0 * kPage, fb);
               bulk_load(sf, p.k_scale + (int64_t)pg0 * kPageSfBytes, kPageSfBytes, fb);
@@ -350,20 +348,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(fb);
           }
         }
-        ++n_issued;
-        if (++stage == kStages) {
-          stage = 0;
-          sphase ^= 1u;
-        }
       }
     }
     if (lane == 0) {
-      for (uint32_t s = 0; s < (uint32_t)kStages; ++s) {
+      // wait for this warp's copies in flight (its stages have parity pw)
+      for (uint32_t s = pw; s < (uint32_t)kStages; s += 2) {
         const uint32_t uses = n_issued > s ? (n_issued - s + kStages - 1) / kStages : 0;
         if (uses) mbar_drain(bar(kBarFull + s), (uses - 1u) & 1u);
       }
-      for (int b = 0; b < 2; ++b)
-        if (q_issued[b]) mbar_drain(bar(kBarQFull + b), (q_issued[b] - 1u) & 1u);
+      if (pw == 0)
+        for (int b = 0; b < 2; ++b)
+          if (q_issued[b]) mbar_drain(bar(kBarQFull + b), (q_issued[b] - 1u) & 1u);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer ----
@@ -535,6 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bar_sync(bar_id, kEpiThreads);
           }
           const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16) + kColAcc + 64u * g;
+          int check_in = kCheckTiles;  // tiles until the next over-limit check
           for (int t = uv.u.t_begin; t < uv.u.t_end; ++t) {
             const uint32_t b = acc_use & 1u;
             const uint32_t ph = (acc_use >> 1) & 1u;
@@ -546,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tb = lane_base + kAccCols * b;
             const int32_t slot = t * kTile + tg;
             const bool in_win = (uint32_t)(slot - s0) < (uint32_t)(e0 - s0);
-            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // four packed (+0, +0) sums
+            uint64_t acc[4];  // four packed partial sums
             // four 16-column TMEM loads, each issued before the previous
             // chunk is reduced (a wait covers every load issued before it)
             uint32_t xa[16], xb[16];
@@ -587,8 +583,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const bool pass = in_win & ((k32 > thi) | ((k32 == thi) & (~(uint32_t)slot >= tlo)));
               const uint64_t key = ((uint64_t)k32 << 32) | (uint64_t)(~(uint32_t)slot);
               over |= sel_append(cand, cnt_s, kCap, kCap - kCheckTiles * kEpiThreads, pass, key);
-              const bool check = ((t - uv.u.t_begin) % kCheckTiles) == kCheckTiles - 1;
-              if (check) {
+              if (--check_in == 0) {
+                check_in = kCheckTiles;
                 if (bar_red_or(bar_id, kEpiThreads, over)) {
                   sel_compact<kEpiThreads, kCap>(cand, cnt_s, tau_s, hist, bc, (uint32_t)TOPK, tg,
                                                  bar_id, hdr);
@@ -627,7 +623,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  if (p.prof && threadIdx.x < 32) atomicAdd(&p.prof[threadIdx.x], prof_s[threadIdx.x]);
 }
 
 template <int MODE, int TOPK>

@@ -141,13 +141,6 @@ int idx_topk_scratch_high_water(int32_t device, uint64_t* bytes);
 int idx_topk_set_timing(int32_t enable);
 int idx_topk_last_timings(float* ms4);
 
-/* Measurement support (no counterpart on the pages): when `device_counters`
- * (device memory, 32 x uint64, caller-owned, zeroed by the caller) is set,
- * every later scoring kernel adds, per wait site, the clock cycles its warps
- * spent waiting on pipeline barriers (warp-summed, lane 0 of each warp) into
- * it.  NULL switches it off (the default).  Process-wide; not thread-safe. */
-int idx_topk_set_wait_profile(void* device_counters);
-
 /*
  * Debug / dense scorer: the same scoring kernel as the fused path, writing the
  * fp32 scores instead of selecting.
