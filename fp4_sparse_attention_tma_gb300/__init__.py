@@ -19,14 +19,16 @@ import ctypes
 
 from . import _lib
 
-__all__ = ["IdxError", "SUPPORTED_K", "idx_topk_fp4_prefill", "idx_dense_topk_fp4_prefill",
+__all__ = ["IdxError", "SUPPORTED_K", "idx_topk_fp4_prefill", "idx_topk_fp4_prefill_noalloc",
+           "idx_dense_topk_fp4_prefill",
            "idx_fp4_debug_scores", "idx_topk_select_scores", "idx_topk_supported_k",
            "idx_topk_status_string", "idx_topk_fp4_scratch_bytes", "idx_topk_scratch_high_water",
            "dense_score_bytes", "STATUS", "idx_topk_set_timing",
            "idx_topk_last_timings"]
 
 STATUS = {0: "OK", 1: "INVALID_ARGUMENT", 2: "UNSUPPORTED", 3: "INVALID_METADATA",
-          4: "INVALID_PAGE", 5: "OVERFLOW", 6: "CUDA_ERROR", 7: "INTERNAL", 8: "TIMEOUT"}
+          4: "INVALID_PAGE", 5: "OVERFLOW", 6: "CUDA_ERROR", 7: "INTERNAL", 8: "TIMEOUT",
+          9: "SCRATCH_LIMIT"}
 SUPPORTED_K = (512, 1024)
 
 _DT = {"uint8": 1, "int32": 2, "float32": 3}
@@ -79,6 +81,19 @@ def idx_topk_fp4_prefill(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_tab
     code = lib.idx_topk_fp4_prefill(*[_ref(d) for d in ds[:9]], int(topk), _ref(ds[9]),
                                     _ref(ds[10]), _stream(stream))
     return _check(code, "idx_topk_fp4_prefill", raise_on_error)
+
+
+def idx_topk_fp4_prefill_noalloc(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table,
+                                 row_req, row_start, row_end, topk, out_phys_slot, out_raw_idx=None,
+                                 stream=None, raise_on_error=True) -> int:
+    """idx_topk_fp4_prefill with its scratch in the library's fixed per-device
+    buffer: allocates nothing; overlapping calls on one device race."""
+    lib = _lib.load()
+    ds = [_desc(t) for t in (q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                             row_start, row_end, out_phys_slot, out_raw_idx)]
+    code = lib.idx_topk_fp4_prefill_noalloc(*[_ref(d) for d in ds[:9]], int(topk), _ref(ds[9]),
+                                            _ref(ds[10]), _stream(stream))
+    return _check(code, "idx_topk_fp4_prefill_noalloc", raise_on_error)
 
 
 def idx_dense_topk_fp4_prefill(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,

@@ -507,6 +507,176 @@ int run(const Call& c, cudaStream_t stream) {
   return IDX_OK;
 }
 
+// ------------------------------------------------ fixed scratch buffer ----
+//
+// Scratch of idx_topk_fp4_prefill_noalloc: one buffer per device inside the
+// library's own device image (placed there when the image is loaded, not
+// allocated by a call).  Its address on a device is looked up once, on the
+// first call that uses the device, with that device current.
+static __device__ __align__(256) unsigned char g_fixed_scratch[IDX_NOALLOC_SCRATCH_BYTES];
+void* g_fixed_ptr[kMaxDevices] = {};
+
+int fixed_scratch(int dev, void** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_fixed_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_fixed_scratch) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return IDX_ERR_CUDA;
+    }
+    g_fixed_ptr[dev] = ptr;
+  }
+  *out = g_fixed_ptr[dev];
+  return IDX_OK;
+}
+
+// SM count and compute capability of `dev`, and the tensor-map encoder; unlike
+// device_state this creates no memory pool.
+int device_info_no_pool(int dev, int* sm, int* major, int* minor) {
+  if (dev < 0 || dev >= kMaxDevices) return IDX_ERR_INVALID_ARGUMENT;
+  if (cudaDeviceGetAttribute(sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return IDX_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr) {
+      cudaGetLastError();
+      return IDX_ERR_CUDA;
+    }
+    g_encode = (EncodeTiledFn)fn;
+  }
+  return IDX_OK;
+}
+
+// The fused path of run() with its scratch taken from the fixed buffer: the
+// same checks, kernels, status read-back and fail-closed behaviour, and no
+// allocation, pool or event creation.
+int run_fixed_scratch(const Call& c, cudaStream_t stream) {
+  Outputs outs;
+  int st = check_output(c.out_phys, c.q_fp4 ? c.q_fp4->shape[0] : 0, c.topk);
+  if (st) return st;
+  outs.t[0] = c.out_phys;
+  if (c.out_raw) {
+    st = check_output(c.out_raw, c.q_fp4 ? c.q_fp4->shape[0] : 0, c.topk);
+    if (st) return st;
+    outs.t[1] = c.out_raw;
+  }
+  const idx_tensor_t* all[] = {c.q_fp4, c.q_scale, c.k_cache_fp4, c.k_scale, c.weights,
+                               c.page_table, c.row_req, c.row_start, c.row_end, c.out_phys,
+                               c.out_raw};
+  int dev = -1;
+  if ((st = common_device(all, 11, &dev))) return st;
+  DeviceGuard guard(dev);
+  if (!guard.ok()) return IDX_ERR_CUDA;
+  st = check_stream(stream, dev);
+  if (st == IDX_ERR_UNSUPPORTED) return st;  // capturing: enqueue nothing
+  auto fail = [&](int code) {
+    fill_minus_one(outs, stream);
+    return code;
+  };
+  if (st) return fail(st);
+  if (!topk_supported(c.topk)) return fail(IDX_ERR_UNSUPPORTED);
+  Sizes sz;
+  st = check_inputs(c.q_fp4, c.q_scale, c.k_cache_fp4, c.k_scale, c.weights, c.page_table,
+                    c.row_req, c.row_start, c.row_end, &sz);
+  if (st) return fail(st);
+  if (sz.rows == 0) return IDX_OK;
+  int sm = 0, major = 0, minor = 0;
+  if ((st = device_info_no_pool(dev, &sm, &major, &minor))) return fail(st);
+  if (!(major == 10 && minor == 3)) return fail(IDX_ERR_UNSUPPORTED);
+  const int grid = sm;
+  Scratch s;
+  s.L = scratch_layout(sz.rows, c.topk, grid, true);
+  if (s.L.total > (size_t)IDX_NOALLOC_SCRATCH_BYTES) return fail(IDX_ERR_SCRATCH_LIMIT);
+  if ((st = fixed_scratch(dev, &s.base))) return fail(st);
+  if (cudaMemsetAsync(s.hdr(), 0, sizeof(PlanHeader), stream) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(IDX_ERR_CUDA);
+  }
+
+  PlanParams pp{};
+  pp.row_req = (const int32_t*)c.row_req->data;
+  pp.row_start = (const int32_t*)c.row_start->data;
+  pp.row_end = (const int32_t*)c.row_end->data;
+  pp.page_table = (const int32_t*)c.page_table->data;
+  pp.rows = (int32_t)sz.rows;
+  pp.num_req = (int32_t)sz.num_req;
+  pp.max_pages = (int32_t)sz.max_pages;
+  pp.num_pages = (int32_t)sz.num_pages;
+  pp.score_thr = c.topk;
+  pp.grid = grid;
+  pp.check_end_le = -1;
+  pp.max_units = s.L.max_units;
+  pp.max_row_slots = s.L.max_row_slots;
+  pp.hdr = s.hdr();
+  pp.row_block = s.at<int32_t>(s.L.row_block);
+  pp.blocks = s.at<BlockInfo>(s.L.blocks);
+  pp.units = s.at<UnitInfo>(s.L.units);
+  pp.sched = s.at<int32_t>(s.L.sched);
+  int cuda_err = launch_plan(pp, stream) != cudaSuccess;
+
+  CUtensorMap tmap_k, tmap_q;
+  if (encode_2d_u8(&tmap_k, c.k_cache_fp4->data, (uint64_t)sz.num_pages * kPage, kPage) ||
+      encode_2d_u8(&tmap_q, c.q_fp4->data, (uint64_t)sz.rows * kHeads, kRowsPerChunk * kHeads)) {
+    cudaStreamSynchronize(stream);
+    cudaGetLastError();
+    return fail(IDX_ERR_CUDA);
+  }
+  ScoreParams sp{};
+  sp.q_scale = (const uint8_t*)c.q_scale->data;
+  sp.k_scale = (const uint8_t*)c.k_scale->data;
+  sp.weights = (const float*)c.weights->data;
+  sp.page_table = pp.page_table;
+  sp.row_start = pp.row_start;
+  sp.row_end = pp.row_end;
+  sp.rows = pp.rows;
+  sp.max_pages = pp.max_pages;
+  sp.num_pages = pp.num_pages;
+  sp.topk = c.topk;
+  sp.mode = kModeSelect;
+  sp.score_thr = pp.score_thr;
+  sp.hdr = pp.hdr;
+  sp.blocks = pp.blocks;
+  sp.units = pp.units;
+  sp.sched = pp.sched;
+  sp.cand_cnt = s.at<uint32_t>(s.L.cand_cnt);
+  sp.cand_keys = s.at<uint64_t>(s.L.cand_keys);
+  cuda_err |= launch_score(tmap_k, tmap_q, sp, grid, stream) != cudaSuccess;
+
+  FinishParams fp{};
+  fp.row_req = pp.row_req;
+  fp.row_start = pp.row_start;
+  fp.row_end = pp.row_end;
+  fp.page_table = pp.page_table;
+  fp.rows = pp.rows;
+  fp.max_pages = pp.max_pages;
+  fp.topk = c.topk;
+  fp.hdr = pp.hdr;
+  fp.row_block = pp.row_block;
+  fp.blocks = pp.blocks;
+  fp.cand_cnt = sp.cand_cnt;
+  fp.cand_keys = sp.cand_keys;
+  fp.out_phys = (int32_t*)c.out_phys->data;
+  fp.out_raw = c.out_raw ? (int32_t*)c.out_raw->data : nullptr;
+  cuda_err |= launch_finish(fp, stream) != cudaSuccess;
+
+  // pageable destination: returns once all of the call's work has completed
+  uint32_t status = 0;
+  if (cudaMemcpyAsync(&status, s.hdr(), sizeof(uint32_t), cudaMemcpyDeviceToHost, stream) !=
+      cudaSuccess)
+    cuda_err = 1;
+  if (cuda_err || cudaGetLastError() != cudaSuccess) return fail(IDX_ERR_CUDA);
+  if (status != kOk) return fail((int)status);
+  return IDX_OK;
+}
+
 const int32_t kSupportedK[2] = {512, 1024};
 
 }  // namespace
@@ -523,6 +693,18 @@ int idx_topk_fp4_prefill(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
   Call c{q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req, row_start, row_end,
          topk, out_phys_slot, out_raw_idx, nullptr, nullptr, Path::kFused};
   return run(c, (cudaStream_t)stream);
+}
+
+int idx_topk_fp4_prefill_noalloc(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                                 const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
+                                 const idx_tensor_t* weights, const idx_tensor_t* page_table,
+                                 const idx_tensor_t* row_req, const idx_tensor_t* row_start,
+                                 const idx_tensor_t* row_end, int32_t topk,
+                                 const idx_tensor_t* out_phys_slot,
+                                 const idx_tensor_t* out_raw_idx, idx_stream_t stream) {
+  Call c{q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req, row_start, row_end,
+         topk, out_phys_slot, out_raw_idx, nullptr, nullptr, Path::kFused};
+  return run_fixed_scratch(c, (cudaStream_t)stream);
 }
 
 int idx_dense_topk_fp4_prefill(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
@@ -625,6 +807,7 @@ const char* idx_topk_status_string(int code) {
     case IDX_ERR_CUDA: return "CUDA error";
     case IDX_ERR_INTERNAL: return "internal selector failure";
     case IDX_ERR_TIMEOUT: return "device wait timed out";
+    case IDX_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the fixed buffer holds";
     default: return "unknown status";
   }
 }

@@ -70,8 +70,10 @@ typedef enum {
   IDX_ERR_CUDA = 6,             /* a CUDA runtime/driver call failed */
   IDX_ERR_INTERNAL = 7,         /* selector failure: a scored row produced fewer than topk
                                    candidates, or a plan bound was exceeded */
-  IDX_ERR_TIMEOUT = 8           /* a bounded device-side wait expired (the kernel returned
+  IDX_ERR_TIMEOUT = 8,          /* a bounded device-side wait expired (the kernel returned
                                    instead of hanging) */
+  IDX_ERR_SCRATCH_LIMIT = 9     /* idx_topk_fp4_prefill_noalloc only: the call needs more
+                                   scratch than IDX_NOALLOC_SCRATCH_BYTES */
 } idx_status_t;
 
 typedef enum { IDX_U8 = 1, IDX_I32 = 2, IDX_F32 = 3 } idx_dtype_t;
@@ -113,6 +115,41 @@ int idx_topk_fp4_prefill(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
                          const idx_tensor_t* row_end, int32_t topk,
                          const idx_tensor_t* out_phys_slot, const idx_tensor_t* out_raw_idx,
                          idx_stream_t stream);
+
+/*
+ * Allocation-free variant of idx_topk_fp4_prefill (the pages have no
+ * counterpart; it exists for callers that must not allocate device memory
+ * during a call: a serving process that has handed all free HBM to its own
+ * caches and allocator, so a new reservation would fail or evict; or a caller
+ * that cannot afford the device synchronisation and driver work that growing
+ * a memory pool may cost inside a latency-bound loop).
+ *
+ * Arguments, layouts, results, ownership and error behaviour are those of
+ * idx_topk_fp4_prefill, with one difference: the scratch comes from a fixed
+ * buffer of IDX_NOALLOC_SCRATCH_BYTES per device that is part of the
+ * library's device image, so the call makes no cudaMalloc/cudaFree, pool or
+ * event allocation.  Its size need is idx_topk_fp4_scratch_bytes(rows, topk):
+ * (rows + 12 * SMs) * topk * 8 bytes plus a few KB; a call that needs more
+ * returns IDX_ERR_SCRATCH_LIMIT (outputs filled with -1) without running.
+ * At 152 SMs that admits up to about 4,280 rows at topk 1024 and 10,290 at 512.
+ *
+ *  - The first call on a device looks up the buffer's address there (the
+ *    device is made current for it); make that first call before any stream
+ *    capture begins.
+ *  - All calls on one device share the one buffer: calls that overlap in time
+ *    on that device (other streams, other host threads) race on it and give
+ *    undefined results.  Serialise them.
+ *  - The call returns after its work on `stream` has completed, like the
+ *    allocating entry point, so back-to-back calls from one thread are safe.
+ */
+#define IDX_NOALLOC_SCRATCH_BYTES (48u * 1024u * 1024u)
+int idx_topk_fp4_prefill_noalloc(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                                 const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
+                                 const idx_tensor_t* weights, const idx_tensor_t* page_table,
+                                 const idx_tensor_t* row_req, const idx_tensor_t* row_start,
+                                 const idx_tensor_t* row_end, int32_t topk,
+                                 const idx_tensor_t* out_phys_slot,
+                                 const idx_tensor_t* out_raw_idx, idx_stream_t stream);
 
 /* The supported topk values, {512, 1024} (aiter#5309 Implementation: explicit
  * supported-K contract).  *ks points to static storage.  Always IDX_OK unless
