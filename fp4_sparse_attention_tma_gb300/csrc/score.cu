@@ -68,7 +68,8 @@ static_assert(kOffSfaAtom % 128 == 0 && kOffSfbAtom % 128 == 0 && kOffCand % 16 
               "alignment");
 
 // misc region
-constexpr uint32_t kMiscTmem = 0, kMiscAbort = 4, kMiscCnt = 8, kMiscTau = 32, kMiscBc = 64;
+constexpr uint32_t kMiscTmem = 0, kMiscAbort = 4, kMiscCnt = 8, kMiscTau = 32, kMiscBc = 64,
+                   kMiscWc = 128;  // [3 rows][4 warps] region counts
 
 // barriers (8 bytes each)
 constexpr int kBarFull = 0;                                  // [kStages]
@@ -95,12 +96,18 @@ static_assert(kColSfb + 2 * 4 * kSfbAtoms <= kTmemCols, "TMEM budget");
 constexpr uint32_t kIdescK0 = idesc_mxf4(128, kAccCols, 0);
 constexpr uint32_t kIdescK1 = idesc_mxf4(128, kAccCols, 2);
 
-// Per-row candidate buffer (keys); compaction is checked every kCheckTiles
-// tiles, each adding at most 128 keys per row, so the buffer keeps
-// kCheckTiles*128 free entries above topk.
+// Per-row candidate buffer of order keys: entries [0, topk) hold the keys kept
+// by the last compaction; behind them each of the row's four epilogue warps
+// appends into a region of its own (warp_region entries), counting in a
+// register, so appending needs no shared-memory atomics.  Every kCheckTiles
+// tiles the warps vote; when a region has less than kCheckTiles * 32 entries
+// free, the group gathers all keys behind the kept ones and compacts them.
 constexpr int kCheckTiles = 8;
-__host__ __device__ constexpr uint32_t cand_cap(int topk) { return topk > 0 ? 2560u : 0u; }
-static_assert(1024 + kCheckTiles * 128 <= 2560, "candidate buffer too small for topk 1024");
+__host__ __device__ constexpr uint32_t cand_cap(int topk) { return topk > 0 ? 3072u : 0u; }
+__host__ __device__ constexpr uint32_t warp_region(int topk) { return (cand_cap(topk) - (uint32_t)topk) / 4u; }
+static_assert(warp_region(1024) >= 2 * kCheckTiles * 32 && warp_region(1024) % 32 == 0 &&
+                  warp_region(512) >= 2 * kCheckTiles * 32 && warp_region(512) % 32 == 0,
+              "candidate regions too small");
 
 __host__ __device__ constexpr size_t smem_bytes_for(int mode, int topk) {
   return 1024 + kOffCand +
@@ -169,6 +176,43 @@ __device__ __forceinline__ float head_sum_final(const uint64_t (&acc)[4]) {
                b1 = unpack2(acc[3]);
   // + 0 turns an all-zero total of -0 into +0, the value a sum started at +0 has
   return (((a0.x + a0.y) + (a1.x + a1.y)) + ((b0.x + b0.y) + (b1.x + b1.y))) + 0.0f;
+}
+
+// Moves the keys the row's four warps appended to their regions directly
+// behind the kept ones, so that the candidates are buf[0, n) again, and stores
+// n in *cnt_s.  Collective over the row's 128 epilogue threads (named barrier
+// bar_id); `wcnt` is the calling warp's region count, `qd` its index.
+template <int TOPK>
+__device__ __noinline__ void sel_gather(uint64_t* buf, uint32_t* cnt_s, uint32_t* wc_s,
+                                        uint32_t wcnt, int qd, int lane, uint32_t bar_id) {
+  constexpr uint32_t kQ = warp_region(TOPK);
+  constexpr int kPer = (int)(kQ / 32);
+  if (lane == 0) wc_s[qd] = wcnt;
+  bar_sync(bar_id, kEpiThreads);
+  const uint32_t kept = *(volatile uint32_t*)cnt_s;
+  uint32_t pre = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const uint32_t c = ((volatile uint32_t*)wc_s)[w];
+    pre += w < qd ? c : 0u;
+    total += c;
+  }
+  const uint64_t* src = buf + TOPK + (uint32_t)qd * kQ;
+  uint64_t v[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    const uint32_t i = (uint32_t)lane + 32u * (uint32_t)e;
+    v[e] = i < wcnt ? src[i] : 0ull;
+  }
+  bar_sync(bar_id, kEpiThreads);  // every region read before any is overwritten
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    const uint32_t i = (uint32_t)lane + 32u * (uint32_t)e;
+    if (i < wcnt) buf[kept + pre + i] = v[e];
+  }
+  bar_sync(bar_id, kEpiThreads);
+  if (qd == 0 && lane == 0) *cnt_s = kept + total;
+  bar_sync(bar_id, kEpiThreads);
 }
 
 struct UnitView {
@@ -474,6 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* cnt_s = reinterpret_cast<uint32_t*>(smem + kOffMisc + kMiscCnt) + g;
     uint64_t* tau_s = reinterpret_cast<uint64_t*>(smem + kOffMisc + kMiscTau) + g;
     uint32_t* bc = reinterpret_cast<uint32_t*>(smem + kOffMisc + kMiscBc) + 4 * g;
+    uint32_t* wc_s = reinterpret_cast<uint32_t*>(smem + kOffMisc + kMiscWc) + 4 * g;
     uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kOffHist) + 256 * g;
     uint64_t* cand = reinterpret_cast<uint64_t*>(smem + kOffCand) + (size_t)g * kCap;
     uint32_t acc_use = 0;
@@ -521,7 +566,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           };
           load_w2();
           uint32_t thi = 0, tlo = 0;  // threshold key (score key, ~index)
-          bool over = false;
+          uint32_t wcnt = 0;          // keys in this warp's append region
+          uint64_t* wreg = cand + TOPK + (uint32_t)qd * warp_region(TOPK);
           if constexpr (MODE == kModeSelect) {
             if (tg == 0) {
               *cnt_s = 0;
@@ -582,10 +628,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t k32 = score_key(sc);
               const bool pass = in_win & ((k32 > thi) | ((k32 == thi) & (~(uint32_t)slot >= tlo)));
               const uint64_t key = ((uint64_t)k32 << 32) | (uint64_t)(~(uint32_t)slot);
-              over |= sel_append(cand, cnt_s, kCap, kCap - kCheckTiles * kEpiThreads, pass, key);
+              const uint32_t m = __ballot_sync(0xffffffffu, pass);
+              if (pass) wreg[wcnt + (uint32_t)__popc(m & ((1u << lane) - 1u))] = key;
+              wcnt += (uint32_t)__popc(m);
               if (--check_in == 0) {
                 check_in = kCheckTiles;
+                const bool over = wcnt > warp_region(TOPK) - kCheckTiles * 32u;
                 if (bar_red_or(bar_id, kEpiThreads, over)) {
+                  sel_gather<TOPK>(cand, cnt_s, wc_s, wcnt, qd, lane, bar_id);
+                  wcnt = 0;
                   sel_compact<kEpiThreads, kCap>(cand, cnt_s, tau_s, hist, bc, (uint32_t)TOPK, tg,
                                                  bar_id, hdr);
                   const uint64_t tk = *(volatile uint64_t*)tau_s;
@@ -593,14 +644,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                   tlo = (uint32_t)(tk & 0xffffffffu);
                   load_w2();  // the weights are not kept live across the compaction
                 }
-                over = false;
               }
             }
           }
           if constexpr (MODE == kModeSelect) {
             if (ok) {
               const int64_t slot_idx = uv.b.slot0 + (int64_t)uv.u.k * uv.b.nrows + g;
-              bar_sync(bar_id, kEpiThreads);
+              sel_gather<TOPK>(cand, cnt_s, wc_s, wcnt, qd, lane, bar_id);
               sel_compact<kEpiThreads, kCap>(cand, cnt_s, tau_s, hist, bc, (uint32_t)TOPK, tg, bar_id,
                                              hdr);
               const uint32_t n = min(*(volatile uint32_t*)cnt_s, (uint32_t)TOPK);
