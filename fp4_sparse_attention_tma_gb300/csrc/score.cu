@@ -18,10 +18,11 @@
 // "[FlyDSL][DSv4] Prototype FP4 MQA streaming TopK" (ROCm/aiter#5282, Changes
 // and Scope), re-designed around TMA, tcgen05 and TMEM.
 //
-// Warp roles (512 threads): warps 0 and 3 TMA producers (alternate K tiles), warp 1 TMEM allocator + MMA
-// issuer (one thread), warp 2 rearranges the query block's and each K tile's
-// scale factors into the TMEM copy layout, warps 4..15 epilogue (warpgroup g = row g of the block; warp w reads
-// TMEM lanes 32*(w%4) .. 32*(w%4)+31, i.e. slots of the tile).
+// Warp roles (512 threads): warps 0 and 3 TMA producers (alternate K tiles;
+// each also rearranges its tiles' scale factors into the TMEM copy layout),
+// warps 1 and 2 MMA issuers (one accumulator buffer each; warp 1 also owns the
+// TMEM allocation), warps 4..15 epilogue (warpgroup g = row g of the block;
+// warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31, i.e. slots of the tile).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -39,10 +40,10 @@ constexpr int kStages = 12;      // K-tile ring (TMA latency x tile rate)
 constexpr int kEpiWarp0 = 4;
 constexpr int kProducer2 = 3;  // second TMA producer warp
 static_assert(kStages % 2 == 0, "producers own the stages of one parity each");
+static_assert(kAccStages == 2, "one MMA issuer warp per accumulator buffer");
 constexpr int kEpiThreads = 128;  // one warpgroup
 
 constexpr uint32_t kPageBytes = kPage * kDimBytes;                 // 4096
-constexpr uint32_t kPageSfBytes = kPage * kNumSF;                  // 256
 constexpr uint32_t kABytes = kTile * kDimBytes;                    // 8192
 constexpr uint32_t kRowBBytes = kHeads * kDimBytes;                // 4096 (one query row)
 constexpr uint32_t kBBytes = kRowsPerBlock * kRowBBytes;           // 12288
@@ -53,11 +54,10 @@ constexpr uint32_t kBlockWBytes = kRowsPerBlock * kHeads * 4;      // 768
 
 constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + kStages * kABytes;
-constexpr uint32_t kOffSfaRaw = kOffB + 2 * kBBytes;
-constexpr uint32_t kOffSfaAtom = kOffSfaRaw + kStages * 512;
-constexpr uint32_t kOffSfbRaw = kOffSfaAtom + kStages * 512;
-constexpr uint32_t kOffSfbAtom = kOffSfbRaw + 2 * kSfbAtomBytes;   // raw region padded to atoms
-constexpr uint32_t kOffW = kOffSfbAtom + 2 * kSfbAtomBytes;
+constexpr uint32_t kOffSfaAtom = kOffB + 2 * kBBytes;               // [kStages] K-tile scale atoms
+constexpr uint32_t kOffSfbRaw = kOffSfaAtom + kStages * 512;        // [2 q buffers], padded to atoms
+constexpr uint32_t kOffSfbAtom = kOffSfbRaw + 2 * kSfbAtomBytes;    // [2 issuers][2 q buffers]
+constexpr uint32_t kOffW = kOffSfbAtom + 2 * 2 * kSfbAtomBytes;
 constexpr uint32_t kOffBar = kOffW + 2 * kBlockWBytes;
 constexpr uint32_t kOffMisc = kOffBar + 512;
 constexpr uint32_t kOffHist = kOffMisc + 256;
@@ -74,15 +74,13 @@ constexpr uint32_t kMiscTmem = 0, kMiscAbort = 4, kMiscCnt = 8, kMiscTau = 32, k
 // barriers (8 bytes each)
 constexpr int kBarFull = 0;                                  // [kStages]
 constexpr int kBarEmpty = kBarFull + kStages;                // [kStages]
-constexpr int kBarSfReady = kBarEmpty + kStages;             // [kStages]
-constexpr int kBarAccFull = kBarSfReady + kStages;           // [kAccStages]
+constexpr int kBarAccFull = kBarEmpty + kStages;             // [kAccStages]
 constexpr int kBarAccEmpty = kBarAccFull + kAccStages;       // [kAccStages]
-constexpr int kBarSfbReady = kBarAccEmpty + kAccStages;      // [2]
-constexpr int kBarQFull = kBarSfbReady + 2;                  // [2]
+constexpr int kBarQFull = kBarAccEmpty + kAccStages;         // [2]
 constexpr int kBarQEmpty = kBarQFull + 2;                    // [2]
 constexpr int kBarEpiDone = kBarQEmpty + 2;                  // [2]
-constexpr int kBarMmaFinal = kBarEpiDone + 2;
-static_assert((kBarMmaFinal + 1) * 8 <= 512, "barrier region");
+constexpr int kBarMmaFinal = kBarEpiDone + 2;                // [kAccStages]
+static_assert((kBarMmaFinal + kAccStages) * 8 <= 512, "barrier region");
 
 
 // TMEM columns
@@ -90,8 +88,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = kRowsPerBlock * kHeads;  // 192: one accumulator buffer
 constexpr uint32_t kColAcc = 0;                      // + kAccCols * stage + 64 * row
 constexpr uint32_t kColSfa = kAccStages * kAccCols;  // 384: + 4 * K stage
-constexpr uint32_t kColSfb = kColSfa + 4 * kStages;  // + 4 * kSfbAtoms * q-buffer (+ 2 * row)
-static_assert(kColSfb + 2 * 4 * kSfbAtoms <= kTmemCols, "TMEM budget");
+constexpr uint32_t kColSfb = kColSfa + 4 * kStages;  // + 4 * kSfbAtoms * (2 * issuer + q buffer)
+static_assert(kColSfb + 2 * 2 * 4 * kSfbAtoms <= kTmemCols, "TMEM budget");
 
 constexpr uint32_t kIdescK0 = idesc_mxf4(128, kAccCols, 0);
 constexpr uint32_t kIdescK1 = idesc_mxf4(128, kAccCols, 2);
@@ -247,19 +245,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kBarFull + s), 1);
       mbar_init(bar(kBarEmpty + s), 1);
-      mbar_init(bar(kBarSfReady + s), 1);
     }
     for (int c = 0; c < kAccStages; ++c) {
       mbar_init(bar(kBarAccFull + c), 1);
       mbar_init(bar(kBarAccEmpty + c), kRowsPerBlock * kEpiThreads);
+      mbar_init(bar(kBarMmaFinal + c), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(kBarQFull + b), 1);
-      mbar_init(bar(kBarQEmpty + b), 1);
-      mbar_init(bar(kBarSfbReady + b), 1);
+      mbar_init(bar(kBarQEmpty + b), kAccStages);  // one commit per MMA issuer
       mbar_init(bar(kBarEpiDone + b), (kThreads / 32) - kEpiWarp0);
     }
-    mbar_init(bar(kBarMmaFinal), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -278,15 +274,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 || warp == kProducer2) {
     // ----------------------------------------------------- TMA producers ----
     // Two warps share the K ring: tile n of the CTA's sequence (stage
-    // n % kStages) is issued by warp 0 when n is even and by the second
-    // producer when n is odd, so two copy streams are in flight at once.  Warp
-    // 0 also loads each unit's query block.
+    // n % kStages) is handled by warp 0 when n is even and by the second
+    // producer when n is odd.  Per tile the warp rearranges the two pages'
+    // UE8M0 scales into the TMEM copy layout itself (operand row r of the
+    // 128-row atom -> 32-bit word 4*(r%32) + r/32; lane i holds rows i, 32+i,
+    // 64+i, 96+i), read one own tile ahead with plain loads, and issues the
+    // two 4 KB page copies.  Warp 0 also loads each unit's query block.
     const uint32_t pw = warp == 0 ? 0u : 1u;
     if (lane == 0 && pw == 0) {
       prefetch_tmap(&tmap_k);
       prefetch_tmap(&tmap_q);
     }
-    uint32_t stage = 0, sphase = 0;
+    const uint32_t* kscale = reinterpret_cast<const uint32_t*>(p.k_scale);  // [page][slot] words
     uint32_t n_issued = 0;  // K tiles of the CTA's sequence so far (both producers)
     uint32_t q_issued[2] = {0, 0};
     bool ok = true;
@@ -336,58 +335,81 @@ __global__ void __launch_bounds__(kThreads, 1)
         ws[j] = aj ? __shfl_sync(0xffffffffu, rs, j) : 0;
         we[j] = aj ? __shfl_sync(0xffffffffu, re, j) : 0;
       }
-      // page-table entries of 32 consecutive logical pages, one per lane,
-      // read only for pages that some row's window touches
+      // page-table entries of 32 consecutive logical pages, one per lane, read
+      // only for pages that some row's window touches; the window always
+      // covers the current tile and the warp's next one (two tiles later)
       int32_t pt_base = -64, pt_val = -1;
       uint32_t pt_need = 0;
+      auto pages_of = [&](int tt, int32_t& pg0, int32_t& pg1, bool& need0, bool& need1) {
+        const int32_t lp0 = 2 * tt, lp1 = 2 * tt + 1;
+        need0 = (pt_need >> (lp0 - pt_base)) & 1u;
+        need1 = (pt_need >> (lp1 - pt_base)) & 1u;
+        const int32_t e0v = __shfl_sync(0xffffffffu, pt_val, lp0 - pt_base);
+        const int32_t e1v = __shfl_sync(0xffffffffu, pt_val, lp1 - pt_base);
+        pg0 = need0 ? e0v : -1;
+        pg1 = need1 ? e1v : -1;
+      };
+      auto load_scales = [&](int32_t pg0, int32_t pg1, uint32_t (&w)[4]) {
+        const bool v0 = pg0 >= 0 && pg0 < p.num_pages, v1 = pg1 >= 0 && pg1 < p.num_pages;
+        w[0] = v0 ? kscale[(int64_t)pg0 * kPage + lane] : 0u;
+        w[1] = v0 ? kscale[(int64_t)pg0 * kPage + 32 + lane] : 0u;
+        w[2] = v1 ? kscale[(int64_t)pg1 * kPage + lane] : 0u;
+        w[3] = v1 ? kscale[(int64_t)pg1 * kPage + 32 + lane] : 0u;
+      };
+      uint32_t wnext[4] = {0u, 0u, 0u, 0u};
+      bool have_next = false;
       for (int t = uv.u.t_begin; t < uv.u.t_end; ++t) {
-        const bool mine = (n_issued & 1u) == pw;
-        const uint32_t st = stage, sp = sphase;
-        ++n_issued;
-        if (++stage == kStages) {
-          stage = 0;
-          sphase ^= 1u;
-        }
-        if (!mine) continue;
-        const int32_t lp0 = 2 * t, lp1 = 2 * t + 1;
-        if (lp1 >= pt_base + 32) {
-          pt_base = lp0;
+        const uint32_t n = n_issued++;
+        if ((n & 1u) != pw) continue;
+        const uint32_t st = n % kStages, sp = (n / kStages) & 1u;
+        if (2 * t + 5 >= pt_base + 32) {
+          pt_base = 2 * t;
           const int32_t lp = pt_base + lane;
           bool need = false;
 #pragma unroll
           for (int j = 0; j < kRowsPerBlock; ++j)
             need |= ws[j] < (lp + 1) * kPage && we[j] > lp * kPage;
+          need &= lp < p.max_pages;
           pt_need = __ballot_sync(0xffffffffu, need);
           pt_val = need ? row_pt[lp] : -1;
         }
-        const bool need0 = (pt_need >> (lp0 - pt_base)) & 1u;
-        const bool need1 = (pt_need >> (lp1 - pt_base)) & 1u;
-        const int32_t e0v = __shfl_sync(0xffffffffu, pt_val, lp0 - pt_base);
-        const int32_t e1v = __shfl_sync(0xffffffffu, pt_val, lp1 - pt_base);
+        int32_t pg0, pg1;
+        bool need0, need1;
+        pages_of(t, pg0, pg1, need0, need1);
+        uint32_t wcur[4];
+        if (have_next) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) wcur[k] = wnext[k];
+        } else {
+          load_scales(pg0, pg1, wcur);
+        }
+        have_next = t + 2 < uv.u.t_end;
+        if (have_next) {
+          int32_t ng0, ng1;
+          bool nn0, nn1;
+          pages_of(t + 2, ng0, ng1, nn0, nn1);
+          load_scales(ng0, ng1, wnext);
+        }
         if (!wait(bar(kBarEmpty + st), sp ^ 1u, 302)) {
           ok = false;
           break;
         }
+        // the stage's previous scale atom was read by the MMA that released it
+        *reinterpret_cast<uint4*>(smem + kOffSfaAtom + st * 512u + 16u * lane) =
+            make_uint4(wcur[0], wcur[1], wcur[2], wcur[3]);
+        fence_proxy_async_smem();
+        __syncwarp();
         if (lane == 0) {
           const uint32_t fb = bar(kBarFull + st);
-          const int32_t pg0 = need0 ? e0v : -1;
-          const int32_t pg1 = need1 ? e1v : -1;
           const bool v0 = need0 && pg0 >= 0 && pg0 < p.num_pages;
           const bool v1 = need1 && pg1 >= 0 && pg1 < p.num_pages;
           if ((need0 && !v0) || (need1 && !v1)) raise_status(hdr, kErrInvalidPage, 303);
-          const uint32_t bytes = ((uint32_t)v0 + (uint32_t)v1) * (kPageBytes + kPageSfBytes);
+          const uint32_t bytes = ((uint32_t)v0 + (uint32_t)v1) * kPageBytes;
           if (bytes) {
             mbar_arrive_expect_tx(fb, bytes);
             const uint32_t a = sbase + kOffA + st * kABytes;
-            const uint32_t sf = sbase + kOffSfaRaw + st * 512u;
-            if (v0) {
-              tma_load_2d(a, &tmap_k, 0, pg0 * kPage, fb);
-              bulk_load(sf, p.k_scale + (int64_t)pg0 * kPageSfBytes, kPageSfBytes, fb);
-            }
-            if (v1) {
-              tma_load_2d(a + kPageBytes, &tmap_k, 0, pg1 * kPage, fb);
-              bulk_load(sf + kPageSfBytes, p.k_scale + (int64_t)pg1 * kPageSfBytes, kPageSfBytes, fb);
-            }
+            if (v0) tma_load_2d(a, &tmap_k, 0, pg0 * kPage, fb);
+            if (v1) tma_load_2d(a + kPageBytes, &tmap_k, 0, pg1 * kPage, fb);
           } else {
             mbar_arrive(fb);
           }
@@ -396,78 +418,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) {
       // wait for this warp's copies in flight (its stages have parity pw)
-      for (uint32_t s = pw; s < (uint32_t)kStages; s += 2) {
-        const uint32_t uses = n_issued > s ? (n_issued - s + kStages - 1) / kStages : 0;
-        if (uses) mbar_drain(bar(kBarFull + s), (uses - 1u) & 1u);
+      for (uint32_t s2 = pw; s2 < (uint32_t)kStages; s2 += 2) {
+        const uint32_t uses = n_issued > s2 ? (n_issued - s2 + kStages - 1) / kStages : 0;
+        if (uses) mbar_drain(bar(kBarFull + s2), (uses - 1u) & 1u);
       }
       if (pw == 0)
-        for (int b = 0; b < 2; ++b)
-          if (q_issued[b]) mbar_drain(bar(kBarQFull + b), (q_issued[b] - 1u) & 1u);
+        for (int b2 = 0; b2 < 2; ++b2)
+          if (q_issued[b2]) mbar_drain(bar(kBarQFull + b2), (q_issued[b2] - 1u) & 1u);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------- MMA issuer ----
-    // One thread issues every tcgen05 operation (scale copies, MMAs,
-    // commits); descriptors and TMEM addresses advance arithmetically.
-    if (lane == 0) {
-      uint32_t stage = 0, sphase = 0, acc_use = 0;
-      const uint64_t a_desc0 = desc_kmajor_sw64(sbase + kOffA);
-      const uint64_t b_desc0 = desc_kmajor_sw64(sbase + kOffB);
-      bool ok = true;
-      for (int i = 0; ok; ++i) {
-        const int ui = blockIdx.x + i * gridDim.x;
-        if (ui >= n_units) break;
-        const UnitInfo u = p.units[p.sched[ui]];
-        const int qb = i & 1;
-        const uint32_t qpar = (uint32_t)(i >> 1) & 1u;
-        // query block landed and its scales rearranged (warp 2)
-        if (!wait(bar(kBarSfbReady + qb), qpar, 310)) break;
-        tc_fence_after();
-        const uint32_t sfb = tmem + kColSfb + 4u * kSfbAtoms * qb;
-        for (uint32_t a = 0; a < kSfbAtoms; ++a)
-          tc_cp_sf(sfb + 4u * a, desc_sf_block(sbase + kOffSfbAtom + qb * kSfbAtomBytes + 512u * a));
-        const uint64_t bd = b_desc0 + ((qb * kBBytes) >> 4);
-        for (int t = u.t_begin; t < u.t_end; ++t) {
-          // K tile landed and its scales rearranged (warp 2)
-          if (!wait(bar(kBarSfReady + stage), sphase, 312)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sfa = tmem + kColSfa + 4u * stage;
-          tc_cp_sf(sfa, desc_sf_block(sbase + kOffSfaAtom + stage * 512u));
-          const uint32_t b = acc_use & 1u;
-          if (!wait(bar(kBarAccEmpty + b), ((acc_use >> 1) & 1u) ^ 1u, 313)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          // all rows of the block in one N = 192 instruction per K step; the
-          // second K = 64 step advances both operands by 32 bytes
-          const uint64_t ad = a_desc0 + ((stage * kABytes) >> 4);
-          const uint32_t d = tmem + kColAcc + kAccCols * b;
-          tc_mma_mxf4(d, ad, bd, kIdescK0, sfa, sfb, 0u);
-          tc_mma_mxf4(d, ad + 2, bd + 2, kIdescK1, sfa, sfb, 1u);
-          tc_commit(bar(kBarAccFull + b));
-          tc_commit(bar(kBarEmpty + stage));
-          ++acc_use;
-          if (++stage == kStages) {
-            stage = 0;
-            sphase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        tc_commit(bar(kBarQEmpty + qb));
-      }
-      tc_commit(bar(kBarMmaFinal));
-      mbar_drain(bar(kBarMmaFinal), 0);
-    }
-    __syncwarp();
-  } else if (warp == 2) {
-    // ------------------------------------------ scale-factor transposer ----
-    // Rearranges UE8M0 scales into the 32x16-byte TMEM copy layout (operand
-    // row n of a 128-row atom -> 32-bit word 4*(n%32) + n/32): the query
-    // block's scales once per unit, each K tile's scales once per tile.
-    uint32_t stage = 0, sphase = 0;
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------ MMA issuers ----
+    // Warp 1 + j issues the tiles n with n % 2 == j, all into accumulator
+    // buffer j: a thread that issues MMAs stalls on its own shared-memory
+    // accesses until they retire, so two issuers hide each other's waits.
+    // Per unit the whole warp rearranges the query block's scales into its own
+    // atom buffer; lane 0 copies them to TMEM and issues the tile MMAs.
+    const uint32_t j = (uint32_t)warp - 1u;
+    uint32_t n_seen = 0, own = 0;
+    const uint64_t a_desc0 = desc_kmajor_sw64(sbase + kOffA);
+    const uint64_t b_desc0 = desc_kmajor_sw64(sbase + kOffB);
     bool ok = true;
     for (int i = 0; ok; ++i) {
       const int ui = blockIdx.x + i * gridDim.x;
@@ -475,39 +444,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       const UnitInfo u = p.units[p.sched[ui]];
       const int qb = i & 1;
       const uint32_t qpar = (uint32_t)(i >> 1) & 1u;
-      if (!wait(bar(kBarQFull + qb), qpar, 331)) break;
-      // the MMA thread's copy of this buffer two units ago has completed
-      if (i >= 2 && !wait(bar(kBarQEmpty + qb), qpar ^ 1u, 332)) break;
+      if (!wait(bar(kBarQFull + qb), qpar, 310)) break;
+      // both issuers' copies from this atom buffer two units ago have completed
+      if (i >= 2 && !wait(bar(kBarQEmpty + qb), qpar ^ 1u, 311)) break;
+      const uint32_t atom_off = kOffSfbAtom + (2u * j + (uint32_t)qb) * kSfbAtomBytes;
       {
         const uint32_t* raw = reinterpret_cast<const uint32_t*>(smem + kOffSfbRaw + qb * kSfbAtomBytes);
-        uint32_t* atom = reinterpret_cast<uint32_t*>(smem + kOffSfbAtom + qb * kSfbAtomBytes);
+        uint32_t* atom = reinterpret_cast<uint32_t*>(smem + atom_off);
 #pragma unroll
         for (int k = 0; k < (int)kSfbAtoms * 4; ++k) {
-          const int a = k >> 2, j = k & 3;  // atom, 32-row group
-          atom[a * 128 + 4 * lane + j] = raw[a * 128 + 32 * j + lane];
+          const int a = k >> 2, jj = k & 3;  // atom, 32-row group
+          atom[a * 128 + 4 * lane + jj] = raw[a * 128 + 32 * jj + lane];
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarSfbReady + qb));
       }
-      for (int t = u.t_begin; t < u.t_end; ++t) {
-        if (!wait(bar(kBarFull + stage), sphase, 330)) {
-          ok = false;
-          break;
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t sfb = tmem + kColSfb + 4u * kSfbAtoms * (2u * j + (uint32_t)qb);
+        for (uint32_t a = 0; a < kSfbAtoms; ++a)
+          tc_cp_sf(sfb + 4u * a, desc_sf_block(sbase + atom_off + 512u * a));
+        const uint64_t bd = b_desc0 + ((qb * kBBytes) >> 4);
+        const uint32_t d = tmem + kColAcc + kAccCols * j;
+        for (int t = u.t_begin; t < u.t_end; ++t) {
+          const uint32_t n = n_seen++;
+          if ((n & 1u) != j) continue;
+          const uint32_t st = n % kStages, sp = (n / kStages) & 1u;
+          // K tile and its scale atom landed
+          if (!wait(bar(kBarFull + st), sp, 312)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa = tmem + kColSfa + 4u * st;
+          tc_cp_sf(sfa, desc_sf_block(sbase + kOffSfaAtom + st * 512u));
+          if (!wait(bar(kBarAccEmpty + j), (own & 1u) ^ 1u, 313)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // all rows of the block in one N = 192 instruction per K step; the
+          // second K = 64 step advances both operands by 32 bytes
+          const uint64_t ad = a_desc0 + ((st * kABytes) >> 4);
+          tc_mma_mxf4(d, ad, bd, kIdescK0, sfa, sfb, 0u);
+          tc_mma_mxf4(d, ad + 2, bd + 2, kIdescK1, sfa, sfb, 1u);
+          tc_commit(bar(kBarAccFull + j));
+          tc_commit(bar(kBarEmpty + st));
+          ++own;
         }
-        const uint32_t* raw = reinterpret_cast<const uint32_t*>(smem + kOffSfaRaw + stage * 512u);
-        uint32_t* atom = reinterpret_cast<uint32_t*>(smem + kOffSfaAtom + stage * 512u);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) atom[4 * lane + j] = raw[32 * j + lane];
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarSfReady + stage));
-        if (++stage == kStages) {
-          stage = 0;
-          sphase ^= 1u;
-        }
+        tc_commit(bar(kBarQEmpty + qb));
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
     }
+    if (lane == 0) {
+      tc_commit(bar(kBarMmaFinal + j));
+      mbar_drain(bar(kBarMmaFinal + j), 0);
+    }
+    __syncwarp();
   } else if (warp >= kEpiWarp0) {
     // --------------------------------------------------------- epilogue ----
     const int g = (warp - kEpiWarp0) >> 2;  // row of the block handled by this warpgroup
