@@ -570,6 +570,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16) + kColAcc + 64u * g;
           int check_in = kCheckTiles;  // tiles until the next over-limit check
+          // The reduction of a tile's sums to its score and the select step
+          // run one tile late, right after the next tile's first TMEM load is
+          // issued, so that their dependent chain overlaps that load and the
+          // next tile's arithmetic.  The first call of a unit is a no-op.
+          uint64_t pacc[4] = {0ull, 0ull, 0ull, 0ull};
+          int32_t pslot = 0;
+          bool pwin = false;
+          auto tail = [&]() {
+            const float sc = head_sum_final(pacc);
+            if constexpr (MODE == kModeDense) {
+              if (pwin) p.dense_out[row * p.dense_stride + pslot] = sc;
+            } else {
+              // cheap 32-bit test first; the low word only decides exact ties
+              const uint32_t k32 = score_key(sc);
+              const bool pass = pwin & ((k32 > thi) | ((k32 == thi) & (~(uint32_t)pslot >= tlo)));
+              const uint64_t key = ((uint64_t)k32 << 32) | (uint64_t)(~(uint32_t)pslot);
+              const uint32_t m = __ballot_sync(0xffffffffu, pass);
+              if (pass) wreg[wcnt + (uint32_t)__popc(m & ((1u << lane) - 1u))] = key;
+              wcnt += (uint32_t)__popc(m);
+            }
+          };
           for (int t = uv.u.t_begin; t < uv.u.t_end; ++t) {
             const uint32_t b = acc_use & 1u;
             const uint32_t ph = (acc_use >> 1) & 1u;
@@ -595,6 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             };
             tmem_ld16(tb, xa);
+            tail();  // previous tile
             tmem_wait_ld16(xa);
             tmem_ld16(tb + 16u, xb);
             dump(xa, 0);
@@ -613,17 +635,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++acc_use;
             dump(xb, 48);
             head_sum_part<24>(xb, w2, acc);
-            const float sc = head_sum_final(acc);
-            if constexpr (MODE == kModeDense) {
-              if (in_win) p.dense_out[row * p.dense_stride + slot] = sc;
-            } else {
-              // cheap 32-bit test first; the low word only decides exact ties
-              const uint32_t k32 = score_key(sc);
-              const bool pass = in_win & ((k32 > thi) | ((k32 == thi) & (~(uint32_t)slot >= tlo)));
-              const uint64_t key = ((uint64_t)k32 << 32) | (uint64_t)(~(uint32_t)slot);
-              const uint32_t m = __ballot_sync(0xffffffffu, pass);
-              if (pass) wreg[wcnt + (uint32_t)__popc(m & ((1u << lane) - 1u))] = key;
-              wcnt += (uint32_t)__popc(m);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) pacc[k] = acc[k];
+            pslot = slot;
+            pwin = in_win;
+            if constexpr (MODE == kModeSelect) {
+              // every kCheckTiles tails the warps vote on compaction (no TMEM
+              // load is in flight here)
               if (--check_in == 0) {
                 check_in = kCheckTiles;
                 const bool over = wcnt > warp_region(TOPK) - kCheckTiles * 32u;
@@ -640,6 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
+          if (ok) tail();  // last tile of the unit
           if constexpr (MODE == kModeSelect) {
             if (ok) {
               const int64_t slot_idx = uv.b.slot0 + (int64_t)uv.u.k * uv.b.nrows + g;
