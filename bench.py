@@ -60,6 +60,24 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of x over all ranks (the slowest rank's time); x itself
+    at world size 1."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flop_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank runs the same workload (weak scaling),
+    so the job does world x the work in the slowest rank's time."""
+    return world * flop_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -269,11 +287,8 @@ def main():
         kern_ms.append(t["kernels_ms"])
     barrier()
     clk = clocks.stop()
-    total = torch.tensor([sum(step_ms)], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(total, op=dist.ReduceOp.MAX)
-    ms_per_step = float(total.item()) / args.steps
-    value = world * flop / (ms_per_step * 1e-3) / 1e12
+    ms_per_step = max_over_ranks(sum(step_ms), world, "cuda") / args.steps
+    value = whole_job_tflops(flop, world, ms_per_step)
 
     # end to end through the public API with host buffers (pinned), copies timed
     pinned = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host.items()}
@@ -296,7 +311,8 @@ def main():
         ev1.synchronize()
         if i >= 2:
             e2e_ms.append(ev0.elapsed_time(ev1))
-    e2e_step = statistics.mean(e2e_ms)
+    barrier()
+    e2e_step = max_over_ranks(statistics.mean(e2e_ms), world, "cuda")
     m.idx_topk_set_timing(False)
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -310,7 +326,7 @@ def main():
                        "parallelism": f"replicas x{world} (rows independent; no collective)"},
             "gpu_launches": 4 * args.steps,
             "clocks": clk,
-            "e2e": {"value": world * flop / (e2e_step * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "e2e": {"value": whole_job_tflops(flop, world, e2e_step), "unit": "TFLOP/s",
                     "ms_per_step": e2e_step, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h}}
 

@@ -36,8 +36,9 @@ __device__ __forceinline__ bool sel_append(uint64_t* buf, uint32_t* cnt, uint32_
   return over;
 }
 
-// Collective over NT threads (tid in [0, NT), named barrier bar_id): reduces
-// the buffer to exactly K keys (those >= the K-th largest) when it holds more.
+// Collective over NT threads (tid in [0, NT), named barrier bar_id, NT a
+// multiple of 32 and at most 256): reduces the buffer to exactly K keys (those
+// >= the K-th largest) when it holds more.
 // The count and tau in shared memory are updated; all threads must call it
 // with the same buffer.  PER = CAP / NT keys per thread are staged in
 // registers during the compaction.
@@ -47,9 +48,38 @@ __device__ __noinline__ void sel_compact(uint64_t* buf, uint32_t* cnt_s, uint64_
                                          uint32_t bar_id, PlanHeader* hdr) {
   const uint32_t n = *(volatile uint32_t*)cnt_s;
   if (n <= K) return;
-  uint64_t prefix = 0, pmask = 0;
+  const int lane = tid & 31, wid = tid >> 5;
+  // Bytes that every key shares need no histogram pass: find the highest bit
+  // in which the keys differ (they are distinct, so one exists).
+  uint64_t kand = ~0ull, kor = 0ull;
+  for (uint32_t i = tid; i < n; i += NT) {
+    const uint64_t k = buf[i];
+    kand &= k;
+    kor |= k;
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    kand &= __shfl_xor_sync(0xffffffffu, kand, o);
+    kor |= __shfl_xor_sync(0xffffffffu, kor, o);
+  }
+  volatile uint64_t* red = reinterpret_cast<volatile uint64_t*>(hist);  // 2 x NT/32 words
+  if (lane == 0) {
+    red[2 * wid] = kand;
+    red[2 * wid + 1] = kor;
+  }
+  bar_sync(bar_id, NT);
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    kand &= red[2 * w];
+    kor |= red[2 * w + 1];
+  }
+  bar_sync(bar_id, NT);  // the words are read before the histogram is cleared
+  const int top = 63 - __clzll((long long)(kand ^ kor));
+  int shift = (top >> 3) << 3;
+  uint64_t pmask = shift == 56 ? 0ull : (~0ull << (shift + 8));
+  uint64_t prefix = kand & pmask;
   uint32_t need = K;
-  for (int shift = 56; shift >= 0; shift -= 8) {
+  for (; shift >= 0; shift -= 8) {
     for (int b = tid; b < 256; b += NT) hist[b] = 0;
     bar_sync(bar_id, NT);
     for (uint32_t i = tid; i < n; i += NT) {
@@ -97,7 +127,6 @@ __device__ __noinline__ void sel_compact(uint64_t* buf, uint32_t* cnt_s, uint64_
   }
   if (tid == 0) bc[3] = 0;
   bar_sync(bar_id, NT);
-  const int lane = tid & 31;
 #pragma unroll
   for (int e = 0; e < PER; ++e) {
     const bool keep = v[e] != 0ull && v[e] >= prefix;
