@@ -36,7 +36,7 @@ namespace idxk {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kStages = 12;      // K-tile ring (TMA latency x tile rate)
+constexpr int kStages = 8;       // K-tile ring (TMA latency x tile rate)
 constexpr int kEpiWarp0 = 4;
 constexpr int kProducer2 = 3;  // second TMA producer warp
 static_assert(kStages % 2 == 0, "producers own the stages of one parity each");
@@ -68,8 +68,9 @@ static_assert(kOffSfaAtom % 128 == 0 && kOffSfbAtom % 128 == 0 && kOffCand % 16 
               "alignment");
 
 // misc region
-constexpr uint32_t kMiscTmem = 0, kMiscAbort = 4, kMiscCnt = 8, kMiscTau = 32, kMiscBc = 64,
-                   kMiscWc = 128;  // [3 rows][4 warps] region counts
+constexpr uint32_t kMiscTmem = 0, kMiscAbort = 4, kMiscTau = 32,
+                   kMiscBc = 64,    // [3 rows][8 words] selection scratch
+                   kMiscWc = 160;   // [3 rows][4 warps] region counts
 
 // barriers (8 bytes each)
 constexpr int kBarFull = 0;                                  // [kStages]
@@ -94,23 +95,29 @@ static_assert(kColSfb + 2 * 2 * 4 * kSfbAtoms <= kTmemCols, "TMEM budget");
 constexpr uint32_t kIdescK0 = idesc_mxf4(128, kAccCols, 0);
 constexpr uint32_t kIdescK1 = idesc_mxf4(128, kAccCols, 2);
 
-// Per-row candidate buffer of order keys: entries [0, topk) hold the keys kept
-// by the last compaction; behind them each of the row's four epilogue warps
-// appends into a region of its own (warp_region entries), counting in a
-// register, so appending needs no shared-memory atomics.  Every kCheckTiles
-// tiles the warps vote; when a region has less than kCheckTiles * 32 entries
-// free, the group gathers all keys behind the kept ones and compacts them.
+// Per-row candidate buffer of order keys, split into one region per epilogue
+// warp of the row (warp_region keys each).  A warp appends its passing keys to
+// its own region, counting in a register (no shared-memory atomics).  Every
+// kCheckTiles tiles the row's warps vote; when a region has fewer than
+// kCheckTiles * 32 entries free, the group finds the threshold that keeps
+// exactly topk keys over all four regions and each warp compacts its own
+// region in place.  A region never has to hold more than topk survivors plus
+// one check window of appends.
 constexpr int kCheckTiles = 8;
-__host__ __device__ constexpr uint32_t cand_cap(int topk) { return topk > 0 ? 3072u : 0u; }
-__host__ __device__ constexpr uint32_t warp_region(int topk) { return (cand_cap(topk) - (uint32_t)topk) / 4u; }
-static_assert(warp_region(1024) >= 2 * kCheckTiles * 32 && warp_region(1024) % 32 == 0 &&
-                  warp_region(512) >= 2 * kCheckTiles * 32 && warp_region(512) % 32 == 0,
-              "candidate regions too small");
+// The candidate buffers take all shared memory the pipeline leaves free.
+constexpr uint32_t kMaxSmem = 227u * 1024u;
+constexpr uint32_t kCandCap = (kMaxSmem - 1024u - kOffCand) / (kRowsPerBlock * 8u) / 128u * 128u;
+__host__ __device__ constexpr uint32_t cand_cap(int topk) { return topk > 0 ? kCandCap : 0u; }
+__host__ __device__ constexpr uint32_t warp_region(int topk) { return cand_cap(topk) / 4u; }
+static_assert(warp_region(1024) >= 1024 + kCheckTiles * 32 && warp_region(1024) % 32 == 0,
+              "a region must hold topk survivors plus one check window");
 
 __host__ __device__ constexpr size_t smem_bytes_for(int mode, int topk) {
   return 1024 + kOffCand +
          (mode == kModeSelect ? (size_t)kRowsPerBlock * cand_cap(topk) * sizeof(uint64_t) : 0);
 }
+
+static_assert(smem_bytes_for(kModeSelect, 1024) <= kMaxSmem, "shared memory budget");
 
 // Bounded wait for the teardown: ignores the abort flag.
 __device__ void mbar_drain(uint32_t bar, uint32_t parity) {
@@ -176,41 +183,114 @@ __device__ __forceinline__ float head_sum_final(const uint64_t (&acc)[4]) {
   return (((a0.x + a0.y) + (a1.x + a1.y)) + ((b0.x + b0.y) + (b1.x + b1.y))) + 0.0f;
 }
 
-// Moves the keys the row's four warps appended to their regions directly
-// behind the kept ones, so that the candidates are buf[0, n) again, and stores
-// n in *cnt_s.  Collective over the row's 128 epilogue threads (named barrier
-// bar_id); `wcnt` is the calling warp's region count, `qd` its index.
+// Collective over a row's four epilogue warps (named barrier bar_id, 128
+// threads): keeps the row's TOPK largest keys over the four regions (region w
+// at buf + w * warp_region(TOPK), holding wc_s[w] keys) and compacts each region
+// in place.  Returns the calling warp's new count; *tau_s receives the kept
+// keys' radix prefix (a lower bound of every kept key) when keys were dropped.
+// The caller has stored its count in wc_s[qd] before a barrier.
 template <int TOPK>
-__device__ __noinline__ void sel_gather(uint64_t* buf, uint32_t* cnt_s, uint32_t* wc_s,
-                                        uint32_t wcnt, int qd, int lane, uint32_t bar_id) {
+__device__ __noinline__ uint32_t sel_compact_regions(uint64_t* buf, const uint32_t* wc_s,
+                                                     uint64_t* tau_s, uint32_t* hist,
+                                                     uint32_t* bc, uint32_t my_cnt, int qd,
+                                                     int lane, uint32_t bar_id, PlanHeader* hdr) {
   constexpr uint32_t kQ = warp_region(TOPK);
-  constexpr int kPer = (int)(kQ / 32);
-  if (lane == 0) wc_s[qd] = wcnt;
+  uint64_t* reg = buf + (uint32_t)qd * kQ;
+  uint32_t n = 0;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) n += ((volatile const uint32_t*)wc_s)[w];
+  if (n <= (uint32_t)TOPK) return my_cnt;
+  // highest bit in which the (distinct) keys differ
+  uint64_t kand = ~0ull, kor = 0ull;
+  for (uint32_t i = lane; i < my_cnt; i += 32) {
+    const uint64_t k = reg[i];
+    kand &= k;
+    kor |= k;
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    kand &= __shfl_xor_sync(0xffffffffu, kand, o);
+    kor |= __shfl_xor_sync(0xffffffffu, kor, o);
+  }
+  volatile uint64_t* red = reinterpret_cast<volatile uint64_t*>(hist);
+  if (lane == 0) {
+    red[2 * qd] = kand;
+    red[2 * qd + 1] = kor;
+  }
   bar_sync(bar_id, kEpiThreads);
-  const uint32_t kept = *(volatile uint32_t*)cnt_s;
-  uint32_t pre = 0, total = 0;
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
-    const uint32_t c = ((volatile uint32_t*)wc_s)[w];
-    pre += w < qd ? c : 0u;
-    total += c;
-  }
-  const uint64_t* src = buf + TOPK + (uint32_t)qd * kQ;
-  uint64_t v[kPer];
-#pragma unroll
-  for (int e = 0; e < kPer; ++e) {
-    const uint32_t i = (uint32_t)lane + 32u * (uint32_t)e;
-    v[e] = i < wcnt ? src[i] : 0ull;
-  }
-  bar_sync(bar_id, kEpiThreads);  // every region read before any is overwritten
-#pragma unroll
-  for (int e = 0; e < kPer; ++e) {
-    const uint32_t i = (uint32_t)lane + 32u * (uint32_t)e;
-    if (i < wcnt) buf[kept + pre + i] = v[e];
+    kand &= red[2 * w];
+    kor |= red[2 * w + 1];
   }
   bar_sync(bar_id, kEpiThreads);
-  if (qd == 0 && lane == 0) *cnt_s = kept + total;
+  const int top = 63 - __clzll((long long)(kand ^ kor));
+  int shift = (top >> 3) << 3;
+  uint64_t pmask = shift == 56 ? 0ull : (~0ull << (shift + 8));
+  uint64_t prefix = kand & pmask;
+  uint32_t need = (uint32_t)TOPK;
+  const int tg = qd * 32 + lane;
+  for (; shift >= 0; shift -= 8) {
+    for (int b2 = tg; b2 < 256; b2 += kEpiThreads) hist[b2] = 0;
+    bar_sync(bar_id, kEpiThreads);
+    for (uint32_t i = lane; i < my_cnt; i += 32) {
+      const uint64_t k = reg[i];
+      if ((k & pmask) == prefix) atomicAdd(&hist[(uint32_t)(k >> shift) & 255u], 1u);
+    }
+    bar_sync(bar_id, kEpiThreads);
+    if (qd == 0) {
+      uint32_t c[8], sum = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        c[e] = hist[255 - 8 * lane - e];
+        sum += c[e];
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      uint32_t above = incl - sum;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (above < need && above + c[e] >= need) {
+          bc[0] = 255u - 8u * lane - e;
+          bc[1] = above;
+          bc[2] = c[e];
+        }
+        above += c[e];
+      }
+    }
+    bar_sync(bar_id, kEpiThreads);
+    const uint32_t d = bc[0], ab = bc[1], cd = bc[2];
+    need -= ab;
+    prefix |= (uint64_t)d << shift;
+    pmask |= (uint64_t)0xffu << shift;
+    if (cd == need) break;
+  }
+  // in place: a kept key moves to an index no higher than the one it was read
+  // from, and a chunk is read before any of its slots is written
+  uint32_t kept = 0;
+  for (uint32_t base = 0; base < my_cnt; base += 32) {
+    const uint32_t i = base + (uint32_t)lane;
+    const uint64_t v = i < my_cnt ? reg[i] : 0ull;
+    const bool keep = i < my_cnt && v >= prefix;
+    const uint32_t m = __ballot_sync(0xffffffffu, keep);
+    if (keep) reg[kept + (uint32_t)__popc(m & ((1u << lane) - 1u))] = v;
+    kept += (uint32_t)__popc(m);
+    __syncwarp();
+  }
+  // every region has been read for the histogram before any warp compacts
+  // (the last barrier above); check the total
+  if (lane == 0) bc[4 + qd] = kept;
   bar_sync(bar_id, kEpiThreads);
+  if (qd == 0 && lane == 0) {
+    if (bc[4] + bc[5] + bc[6] + bc[7] != (uint32_t)TOPK) raise_status(hdr, kErrInternal, 201);
+    *tau_s = prefix;
+  }
+  bar_sync(bar_id, kEpiThreads);
+  return kept;
 }
 
 struct UnitView {
@@ -508,9 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tg = qd * 32 + lane;           // slot within tile == thread in group
     const uint32_t bar_id = 1u + (uint32_t)g;
     constexpr uint32_t kCap = cand_cap(TOPK);
-    uint32_t* cnt_s = reinterpret_cast<uint32_t*>(smem + kOffMisc + kMiscCnt) + g;
     uint64_t* tau_s = reinterpret_cast<uint64_t*>(smem + kOffMisc + kMiscTau) + g;
-    uint32_t* bc = reinterpret_cast<uint32_t*>(smem + kOffMisc + kMiscBc) + 4 * g;
+    uint32_t* bc = reinterpret_cast<uint32_t*>(smem + kOffMisc + kMiscBc) + 8 * g;
     uint32_t* wc_s = reinterpret_cast<uint32_t*>(smem + kOffMisc + kMiscWc) + 4 * g;
     uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kOffHist) + 256 * g;
     uint64_t* cand = reinterpret_cast<uint64_t*>(smem + kOffCand) + (size_t)g * kCap;
@@ -560,12 +639,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           load_w2();
           uint32_t thi = 0, tlo = 0;  // threshold key (score key, ~index)
           uint32_t wcnt = 0;          // keys in this warp's append region
-          uint64_t* wreg = cand + TOPK + (uint32_t)qd * warp_region(TOPK);
+          uint64_t* wreg = cand + (uint32_t)qd * warp_region(TOPK);
           if constexpr (MODE == kModeSelect) {
-            if (tg == 0) {
-              *cnt_s = 0;
-              *tau_s = 0ull;
-            }
+            if (tg == 0) *tau_s = 0ull;
             bar_sync(bar_id, kEpiThreads);
           }
           const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16) + kColAcc + 64u * g;
@@ -645,11 +721,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (--check_in == 0) {
                 check_in = kCheckTiles;
                 const bool over = wcnt > warp_region(TOPK) - kCheckTiles * 32u;
+                if (lane == 0) wc_s[qd] = wcnt;  // visible to the group after the vote
                 if (bar_red_or(bar_id, kEpiThreads, over)) {
-                  sel_gather<TOPK>(cand, cnt_s, wc_s, wcnt, qd, lane, bar_id);
-                  wcnt = 0;
-                  sel_compact<kEpiThreads, kCap>(cand, cnt_s, tau_s, hist, bc, (uint32_t)TOPK, tg,
-                                                 bar_id, hdr);
+                  wcnt = sel_compact_regions<TOPK>(cand, wc_s, tau_s, hist, bc, wcnt, qd, lane,
+                                                   bar_id, hdr);
                   const uint64_t tk = *(volatile uint64_t*)tau_s;
                   thi = (uint32_t)(tk >> 32);
                   tlo = (uint32_t)(tk & 0xffffffffu);
@@ -662,12 +737,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (MODE == kModeSelect) {
             if (ok) {
               const int64_t slot_idx = uv.b.slot0 + (int64_t)uv.u.k * uv.b.nrows + g;
-              sel_gather<TOPK>(cand, cnt_s, wc_s, wcnt, qd, lane, bar_id);
-              sel_compact<kEpiThreads, kCap>(cand, cnt_s, tau_s, hist, bc, (uint32_t)TOPK, tg, bar_id,
-                                             hdr);
-              const uint32_t n = min(*(volatile uint32_t*)cnt_s, (uint32_t)TOPK);
-              uint64_t* dst = p.cand_keys + slot_idx * TOPK;
-              for (uint32_t e = tg; e < n; e += kEpiThreads) dst[e] = cand[e];
+              if (lane == 0) wc_s[qd] = wcnt;
+              bar_sync(bar_id, kEpiThreads);
+              wcnt = sel_compact_regions<TOPK>(cand, wc_s, tau_s, hist, bc, wcnt, qd, lane, bar_id,
+                                               hdr);
+              // the regions' survivors, region by region, to the unit's list
+              if (lane == 0) wc_s[qd] = wcnt;
+              bar_sync(bar_id, kEpiThreads);
+              uint32_t pre = 0, n = 0;
+#pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                const uint32_t c = ((volatile uint32_t*)wc_s)[w];
+                pre += w < qd ? c : 0u;
+                n += c;
+              }
+              uint64_t* dst = p.cand_keys + slot_idx * TOPK + pre;
+              for (uint32_t e = lane; e < wcnt; e += 32) dst[e] = wreg[e];
               if (tg == 0) p.cand_cnt[slot_idx] = n;
               bar_sync(bar_id, kEpiThreads);
             }
