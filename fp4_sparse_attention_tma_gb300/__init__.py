@@ -20,6 +20,7 @@ import ctypes
 from . import _lib
 
 __all__ = ["IdxError", "SUPPORTED_K", "idx_topk_fp4_prefill", "idx_topk_fp4_prefill_noalloc",
+           "idx_topk_fp4_prefill_async",
            "idx_dense_topk_fp4_prefill",
            "idx_fp4_debug_scores", "idx_topk_select_scores", "idx_topk_supported_k",
            "idx_topk_status_string", "idx_topk_fp4_scratch_bytes", "idx_topk_scratch_high_water",
@@ -81,6 +82,23 @@ def idx_topk_fp4_prefill(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_tab
     code = lib.idx_topk_fp4_prefill(*[_ref(d) for d in ds[:9]], int(topk), _ref(ds[9]),
                                     _ref(ds[10]), _stream(stream))
     return _check(code, "idx_topk_fp4_prefill", raise_on_error)
+
+
+def idx_topk_fp4_prefill_async(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table,
+                               row_req, row_start, row_end, topk, out_phys_slot, workspace, status,
+                               out_raw_idx=None, stream=None, raise_on_error=True) -> int:
+    """Stream-ordered call: no host sync, no allocation (graph-capturable).
+    `workspace` is a uint8 device tensor of at least idx_topk_fp4_scratch_bytes
+    bytes; `status` an int32 device tensor of one element that receives the
+    device-side status."""
+    lib = _lib.load()
+    ds = [_desc(t) for t in (q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                             row_start, row_end, out_phys_slot, out_raw_idx)]
+    code = lib.idx_topk_fp4_prefill_async(*[_ref(d) for d in ds[:9]], int(topk), _ref(ds[9]),
+                                          _ref(ds[10]), ctypes.c_void_p(workspace.data_ptr()),
+                                          ctypes.c_uint64(workspace.numel() * workspace.element_size()),
+                                          ctypes.c_void_p(status.data_ptr()), _stream(stream))
+    return _check(code, "idx_topk_fp4_prefill_async", raise_on_error)
 
 
 def idx_topk_fp4_prefill_noalloc(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table,

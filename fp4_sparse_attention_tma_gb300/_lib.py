@@ -80,6 +80,10 @@ EXPORTS = {
     "idx_topk_fp4_prefill": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
                              [ctypes.c_int32, ctypes.POINTER(IdxTensor), ctypes.POINTER(IdxTensor),
                               ctypes.c_void_p]),
+    "idx_topk_fp4_prefill_async": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
+                                   [ctypes.c_int32, ctypes.POINTER(IdxTensor),
+                                    ctypes.POINTER(IdxTensor), ctypes.c_void_p, ctypes.c_uint64,
+                                    ctypes.c_void_p, ctypes.c_void_p]),
     "idx_topk_fp4_prefill_noalloc": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
                                      [ctypes.c_int32, ctypes.POINTER(IdxTensor),
                                       ctypes.POINTER(IdxTensor), ctypes.c_void_p]),

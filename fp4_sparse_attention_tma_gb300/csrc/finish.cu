@@ -162,6 +162,28 @@ cudaError_t launch_finish(const FinishParams& p, cudaStream_t stream) {
   return cudaErrorInvalidValue;
 }
 
+namespace {
+__global__ void publish_status_kernel(const PlanHeader* hdr, uint32_t* status_out,
+                                      int32_t* out_phys, int32_t* out_raw, int64_t n) {
+  const uint32_t st = read_status(hdr);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *status_out = st;
+  if (st == kOk) return;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    out_phys[i] = -1;
+    if (out_raw) out_raw[i] = -1;
+  }
+}
+}  // namespace
+
+cudaError_t launch_publish_status(const PlanHeader* hdr, uint32_t* status_out, int32_t* out_phys,
+                                  int32_t* out_raw, int64_t n, cudaStream_t stream) {
+  const int64_t want = (n + 255) / 256;
+  const int grid = (int)(want < 1 ? 1 : (want > 1024 ? 1024 : want));
+  publish_status_kernel<<<grid, 256, 0, stream>>>(hdr, status_out, out_phys, out_raw, n);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_validate_windows(const int32_t* row_start, const int32_t* row_end, int32_t rows,
                                     int64_t width, PlanHeader* hdr, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;

@@ -677,6 +677,146 @@ int run_fixed_scratch(const Call& c, cudaStream_t stream) {
   return IDX_OK;
 }
 
+// ------------------------------------------------ stream-ordered call ----
+//
+// The fused path with a caller workspace and a device status word: no
+// allocation, no host synchronisation, so it may be captured into a CUDA graph.
+// Host-side argument errors return at once with nothing enqueued; everything
+// the device detects is published to *status_out by the last kernel, which
+// also fills the outputs with -1 in that case.
+int run_stream_ordered(const Call& c, void* workspace, uint64_t workspace_bytes,
+                       uint32_t* status_out, cudaStream_t stream) {
+  int st = check_output(c.out_phys, c.q_fp4 ? c.q_fp4->shape[0] : 0, c.topk);
+  if (st) return st;
+  if (c.out_raw && (st = check_output(c.out_raw, c.q_fp4 ? c.q_fp4->shape[0] : 0, c.topk)))
+    return st;
+  if (!status_out || ((uintptr_t)status_out & 3u) != 0) return IDX_ERR_INVALID_ARGUMENT;
+  const idx_tensor_t* all[] = {c.q_fp4, c.q_scale, c.k_cache_fp4, c.k_scale, c.weights,
+                               c.page_table, c.row_req, c.row_start, c.row_end, c.out_phys,
+                               c.out_raw};
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return IDX_ERR_CUDA;
+  }
+  const bool capturing = cs != cudaStreamCaptureStatusNone;
+  int dev = -1;
+  if (capturing) {
+    // pointer and stream-device queries fail while a stream is captured: the
+    // device is the current one (the caller guarantees that the stream and
+    // the tensors belong to it)
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+      cudaGetLastError();
+      return IDX_ERR_CUDA;
+    }
+  } else {
+    if ((st = common_device(all, 11, &dev))) return st;
+    if (device_of(status_out) != dev) return IDX_ERR_INVALID_ARGUMENT;
+  }
+  DeviceGuard guard(dev);
+  if (!guard.ok()) return IDX_ERR_CUDA;
+  if (stream != nullptr && !capturing) {
+    int sd = -1;
+    if (cudaStreamGetDevice(stream, &sd) != cudaSuccess) {
+      cudaGetLastError();
+      return IDX_ERR_INVALID_ARGUMENT;
+    }
+    if (sd != dev) return IDX_ERR_INVALID_ARGUMENT;
+  }
+  if (!topk_supported(c.topk)) return IDX_ERR_UNSUPPORTED;
+  Sizes sz;
+  if ((st = check_inputs(c.q_fp4, c.q_scale, c.k_cache_fp4, c.k_scale, c.weights, c.page_table,
+                         c.row_req, c.row_start, c.row_end, &sz)))
+    return st;
+  int sm = 0, major = 0, minor = 0;
+  if ((st = device_info_no_pool(dev, &sm, &major, &minor))) return st;
+  if (!(major == 10 && minor == 3)) return IDX_ERR_UNSUPPORTED;
+  const int grid = sm;
+  Scratch s;
+  s.L = scratch_layout(sz.rows, c.topk, grid, true);
+  if (sz.rows > 0) {
+    if (!workspace || ((uintptr_t)workspace & 255u) != 0 || workspace_bytes < s.L.total ||
+        (!capturing && device_of(workspace) != dev))
+      return IDX_ERR_INVALID_ARGUMENT;
+  }
+  if (sz.rows == 0) {
+    return cudaMemsetAsync(status_out, 0, sizeof(uint32_t), stream) == cudaSuccess ? IDX_OK
+                                                                                   : IDX_ERR_CUDA;
+  }
+  s.base = workspace;
+  int cuda_err = cudaMemsetAsync(s.hdr(), 0, sizeof(PlanHeader), stream) != cudaSuccess;
+
+  PlanParams pp{};
+  pp.row_req = (const int32_t*)c.row_req->data;
+  pp.row_start = (const int32_t*)c.row_start->data;
+  pp.row_end = (const int32_t*)c.row_end->data;
+  pp.page_table = (const int32_t*)c.page_table->data;
+  pp.rows = (int32_t)sz.rows;
+  pp.num_req = (int32_t)sz.num_req;
+  pp.max_pages = (int32_t)sz.max_pages;
+  pp.num_pages = (int32_t)sz.num_pages;
+  pp.score_thr = c.topk;
+  pp.grid = grid;
+  pp.check_end_le = -1;
+  pp.max_units = s.L.max_units;
+  pp.max_row_slots = s.L.max_row_slots;
+  pp.hdr = s.hdr();
+  pp.row_block = s.at<int32_t>(s.L.row_block);
+  pp.blocks = s.at<BlockInfo>(s.L.blocks);
+  pp.units = s.at<UnitInfo>(s.L.units);
+  pp.sched = s.at<int32_t>(s.L.sched);
+  cuda_err |= launch_plan(pp, stream) != cudaSuccess;
+
+  CUtensorMap tmap_k, tmap_q;
+  if (encode_2d_u8(&tmap_k, c.k_cache_fp4->data, (uint64_t)sz.num_pages * kPage, kPage) ||
+      encode_2d_u8(&tmap_q, c.q_fp4->data, (uint64_t)sz.rows * kHeads, kRowsPerChunk * kHeads))
+    return IDX_ERR_CUDA;
+  ScoreParams sp{};
+  sp.q_scale = (const uint8_t*)c.q_scale->data;
+  sp.k_scale = (const uint8_t*)c.k_scale->data;
+  sp.weights = (const float*)c.weights->data;
+  sp.page_table = pp.page_table;
+  sp.row_start = pp.row_start;
+  sp.row_end = pp.row_end;
+  sp.rows = pp.rows;
+  sp.max_pages = pp.max_pages;
+  sp.num_pages = pp.num_pages;
+  sp.topk = c.topk;
+  sp.mode = kModeSelect;
+  sp.score_thr = pp.score_thr;
+  sp.hdr = pp.hdr;
+  sp.blocks = pp.blocks;
+  sp.units = pp.units;
+  sp.sched = pp.sched;
+  sp.cand_cnt = s.at<uint32_t>(s.L.cand_cnt);
+  sp.cand_keys = s.at<uint64_t>(s.L.cand_keys);
+  cuda_err |= launch_score(tmap_k, tmap_q, sp, grid, stream) != cudaSuccess;
+
+  FinishParams fp{};
+  fp.row_req = pp.row_req;
+  fp.row_start = pp.row_start;
+  fp.row_end = pp.row_end;
+  fp.page_table = pp.page_table;
+  fp.rows = pp.rows;
+  fp.max_pages = pp.max_pages;
+  fp.topk = c.topk;
+  fp.hdr = pp.hdr;
+  fp.row_block = pp.row_block;
+  fp.blocks = pp.blocks;
+  fp.cand_cnt = sp.cand_cnt;
+  fp.cand_keys = sp.cand_keys;
+  fp.out_phys = (int32_t*)c.out_phys->data;
+  fp.out_raw = c.out_raw ? (int32_t*)c.out_raw->data : nullptr;
+  cuda_err |= launch_finish(fp, stream) != cudaSuccess;
+  cuda_err |= launch_publish_status(pp.hdr, status_out, fp.out_phys, fp.out_raw,
+                                    sz.rows * (int64_t)c.topk, stream) != cudaSuccess;
+  if (cuda_err) {
+    cudaGetLastError();
+    return IDX_ERR_CUDA;
+  }
+  return IDX_OK;
+}
+
 const int32_t kSupportedK[2] = {512, 1024};
 
 }  // namespace
@@ -705,6 +845,19 @@ int idx_topk_fp4_prefill_noalloc(const idx_tensor_t* q_fp4, const idx_tensor_t* 
   Call c{q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req, row_start, row_end,
          topk, out_phys_slot, out_raw_idx, nullptr, nullptr, Path::kFused};
   return run_fixed_scratch(c, (cudaStream_t)stream);
+}
+
+int idx_topk_fp4_prefill_async(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                               const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
+                               const idx_tensor_t* weights, const idx_tensor_t* page_table,
+                               const idx_tensor_t* row_req, const idx_tensor_t* row_start,
+                               const idx_tensor_t* row_end, int32_t topk,
+                               const idx_tensor_t* out_phys_slot, const idx_tensor_t* out_raw_idx,
+                               void* workspace, uint64_t workspace_bytes, uint32_t* status,
+                               idx_stream_t stream) {
+  Call c{q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req, row_start, row_end,
+         topk, out_phys_slot, out_raw_idx, nullptr, nullptr, Path::kFused};
+  return run_stream_ordered(c, workspace, workspace_bytes, status, (cudaStream_t)stream);
 }
 
 int idx_dense_topk_fp4_prefill(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,

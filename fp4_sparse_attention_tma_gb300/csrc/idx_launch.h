@@ -9,6 +9,19 @@
 
 namespace idxk {
 
+// Sets a kernel's dynamic shared-memory limit once per device (the attribute
+// persists, and repeating the call is avoided while a stream is captured).
+template <typename Kernel>
+inline cudaError_t set_smem_once(Kernel kernel, int bytes, bool (&done)[64]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (done[dev]) return cudaSuccess;
+  const cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err == cudaSuccess) done[dev] = true;
+  return err;
+}
+
 // plan_kernel (1 CTA) then validate_pages_kernel.
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 
@@ -27,5 +40,11 @@ cudaError_t launch_finish(const FinishParams& p, cudaStream_t stream);
 // Checks 0 <= start <= end <= width for every row of a bare score matrix.
 cudaError_t launch_validate_windows(const int32_t* row_start, const int32_t* row_end, int32_t rows,
                                     int64_t width, PlanHeader* hdr, cudaStream_t stream);
+
+// Stream-ordered end of a call whose status is not read by the host: copies
+// the status word to `status_out` and, when it is not kOk, fills the n
+// entries of out_phys (and out_raw, when given) with -1.
+cudaError_t launch_publish_status(const PlanHeader* hdr, uint32_t* status_out, int32_t* out_phys,
+                                  int32_t* out_raw, int64_t n, cudaStream_t stream);
 
 }  // namespace idxk

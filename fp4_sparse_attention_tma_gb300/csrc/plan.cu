@@ -295,8 +295,8 @@ __global__ void __launch_bounds__(256) validate_pages_kernel(PlanParams p) {
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
   static const size_t kSortBytes = sizeof(uint64_t) * kSortMax;
-  cudaError_t err = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSortBytes);
+  static bool done[64] = {};
+  cudaError_t err = set_smem_once(plan_kernel, (int)kSortBytes, done);
   if (err != cudaSuccess) return err;
   plan_kernel<<<1, kPlanThreads, kSortBytes, stream>>>(p);
   err = cudaGetLastError();

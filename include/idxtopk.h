@@ -117,6 +117,43 @@ int idx_topk_fp4_prefill(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
                          idx_stream_t stream);
 
 /*
+ * Stream-ordered variant of idx_topk_fp4_prefill for decode loops and CUDA
+ * graphs: the same operation and outputs, with no allocation and no host
+ * synchronisation, so a call may be captured into a graph and replayed.  The
+ * pages keep decode and graph capture on their previous path and name it as
+ * follow-up work ("[FlyDSL][DSv4] Prototype FP4 MQA streaming TopK",
+ * ROCm/aiter#5282, Scope); this entry point is that follow-up.
+ *   workspace        device memory on the tensors' device, 256-byte aligned,
+ *                    at least idx_topk_fp4_scratch_bytes(rows, topk) bytes;
+ *                    caller-owned, must not be used by another call that runs
+ *                    at the same time.
+ *   status           one device uint32 (4-byte aligned) on the same device;
+ *                    after the call's work completes on `stream` it holds
+ *                    IDX_OK or the device-detected error (invalid metadata,
+ *                    invalid page, internal, timeout), and on such an error
+ *                    every output entry is -1.
+ * Returns IDX_OK when the work was enqueued on `stream` (whether or not the
+ * stream is being captured).  Argument errors found on the host (descriptors,
+ * shapes, topk, device, workspace size or alignment) return their code with
+ * nothing enqueued, the outputs and *status untouched; IDX_ERR_CUDA means a
+ * launch failed and *status is not written.  While `stream` is being
+ * captured, pointer and stream-device queries are not allowed, so the call
+ * uses the current device and does not check that the stream and the tensors
+ * belong to it; make one call outside the capture first (it checks them and
+ * performs the library's per-device setup).  Graph
+ * replays reuse the pointers and sizes seen at capture (a new shape needs a
+ * new capture).
+ */
+int idx_topk_fp4_prefill_async(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                               const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
+                               const idx_tensor_t* weights, const idx_tensor_t* page_table,
+                               const idx_tensor_t* row_req, const idx_tensor_t* row_start,
+                               const idx_tensor_t* row_end, int32_t topk,
+                               const idx_tensor_t* out_phys_slot, const idx_tensor_t* out_raw_idx,
+                               void* workspace, uint64_t workspace_bytes, uint32_t* status,
+                               idx_stream_t stream);
+
+/*
  * Allocation-free variant of idx_topk_fp4_prefill (the pages have no
  * counterpart; it exists for callers that must not allocate device memory
  * during a call: a serving process that has handed all free HBM to its own
