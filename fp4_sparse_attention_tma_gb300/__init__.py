@@ -20,7 +20,7 @@ import ctypes
 from . import _lib
 
 __all__ = ["IdxError", "SUPPORTED_K", "idx_topk_fp4_prefill", "idx_topk_fp4_prefill_noalloc",
-           "idx_topk_fp4_prefill_async",
+           "idx_topk_fp4_prefill_async", "idx_topk_fp4_prefill_paged",
            "idx_dense_topk_fp4_prefill",
            "idx_fp4_debug_scores", "idx_topk_select_scores", "idx_topk_supported_k",
            "idx_topk_status_string", "idx_topk_fp4_scratch_bytes", "idx_topk_scratch_high_water",
@@ -82,6 +82,19 @@ def idx_topk_fp4_prefill(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_tab
     code = lib.idx_topk_fp4_prefill(*[_ref(d) for d in ds[:9]], int(topk), _ref(ds[9]),
                                     _ref(ds[10]), _stream(stream))
     return _check(code, "idx_topk_fp4_prefill", raise_on_error)
+
+
+def idx_topk_fp4_prefill_paged(q_fp4, q_scale, k_pages, weights, page_table, row_req, row_start,
+                               row_end, topk, out_phys_slot, out_raw_idx=None, stream=None,
+                               raise_on_error=True) -> int:
+    """idx_topk_fp4_prefill on a page-interleaved K cache u8 [NP, 4352]
+    (each page: 4096 code bytes, then 256 scale bytes)."""
+    lib = _lib.load()
+    ds = [_desc(t) for t in (q_fp4, q_scale, k_pages, weights, page_table, row_req, row_start,
+                             row_end, out_phys_slot, out_raw_idx)]
+    code = lib.idx_topk_fp4_prefill_paged(*[_ref(d) for d in ds[:8]], int(topk), _ref(ds[8]),
+                                          _ref(ds[9]), _stream(stream))
+    return _check(code, "idx_topk_fp4_prefill_paged", raise_on_error)
 
 
 def idx_topk_fp4_prefill_async(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table,

@@ -80,6 +80,9 @@ EXPORTS = {
     "idx_topk_fp4_prefill": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
                              [ctypes.c_int32, ctypes.POINTER(IdxTensor), ctypes.POINTER(IdxTensor),
                               ctypes.c_void_p]),
+    "idx_topk_fp4_prefill_paged": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 8 +
+                                   [ctypes.c_int32, ctypes.POINTER(IdxTensor),
+                                    ctypes.POINTER(IdxTensor), ctypes.c_void_p]),
     "idx_topk_fp4_prefill_async": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
                                    [ctypes.c_int32, ctypes.POINTER(IdxTensor),
                                     ctypes.POINTER(IdxTensor), ctypes.c_void_p, ctypes.c_uint64,

@@ -204,12 +204,18 @@ int check_inputs(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
                  const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
                  const idx_tensor_t* weights, const idx_tensor_t* page_table,
                  const idx_tensor_t* row_req, const idx_tensor_t* row_start,
-                 const idx_tensor_t* row_end, Sizes* sz) {
+                 const idx_tensor_t* row_end, Sizes* sz, const idx_tensor_t* k_pages = nullptr) {
   int st;
   if ((st = check_tensor(q_fp4, IDX_U8, 3))) return st;
   if ((st = check_tensor(q_scale, IDX_U8, 3))) return st;
-  if ((st = check_tensor(k_cache_fp4, IDX_U8, 3))) return st;
-  if ((st = check_tensor(k_scale, IDX_U8, 3))) return st;
+  if (k_pages) {
+    // page-interleaved K cache: [NP, 64 * 64 code bytes + 64 * 4 scale bytes]
+    if ((st = check_tensor(k_pages, IDX_U8, 2))) return st;
+    if (k_pages->shape[1] != kPage * (kDimBytes + kNumSF)) return IDX_ERR_UNSUPPORTED;
+  } else {
+    if ((st = check_tensor(k_cache_fp4, IDX_U8, 3))) return st;
+    if ((st = check_tensor(k_scale, IDX_U8, 3))) return st;
+  }
   if ((st = check_tensor(weights, IDX_F32, 2))) return st;
   if ((st = check_tensor(page_table, IDX_I32, 2))) return st;
   if ((st = check_tensor(row_req, IDX_I32, 1))) return st;
@@ -218,18 +224,19 @@ int check_inputs(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
   // H = 64 heads, D = 128 (64 bytes, 4 scales), page size 64 are the supported
   // specialisation (aiter#5282 Scope)
   if (q_fp4->shape[1] != kHeads || q_fp4->shape[2] != kDimBytes) return IDX_ERR_UNSUPPORTED;
-  if (k_cache_fp4->shape[1] != kPage || k_cache_fp4->shape[2] != kDimBytes) return IDX_ERR_UNSUPPORTED;
+  if (!k_pages && (k_cache_fp4->shape[1] != kPage || k_cache_fp4->shape[2] != kDimBytes))
+    return IDX_ERR_UNSUPPORTED;
   const int64_t R = q_fp4->shape[0];
   if (q_scale->shape[0] != R || q_scale->shape[1] != kHeads || q_scale->shape[2] != kNumSF)
     return IDX_ERR_INVALID_ARGUMENT;
-  if (k_scale->shape[0] != k_cache_fp4->shape[0] || k_scale->shape[1] != kPage ||
-      k_scale->shape[2] != kNumSF)
+  if (!k_pages && (k_scale->shape[0] != k_cache_fp4->shape[0] || k_scale->shape[1] != kPage ||
+                   k_scale->shape[2] != kNumSF))
     return IDX_ERR_INVALID_ARGUMENT;
   if (weights->shape[0] != R || weights->shape[1] != kHeads) return IDX_ERR_INVALID_ARGUMENT;
   if (row_req->shape[0] != R || row_start->shape[0] != R || row_end->shape[0] != R)
     return IDX_ERR_INVALID_ARGUMENT;
   sz->rows = R;
-  sz->num_pages = k_cache_fp4->shape[0];
+  sz->num_pages = k_pages ? k_pages->shape[0] : k_cache_fp4->shape[0];
   sz->num_req = page_table->shape[0];
   sz->max_pages = page_table->shape[1];
   // physical slots and logical positions are int32 (aiter#5309 Implementation:
@@ -300,6 +307,20 @@ int encode_2d_u8(CUtensorMap* map, void* base, uint64_t rows, uint32_t box_rows)
   return r == CUDA_SUCCESS ? IDX_OK : IDX_ERR_CUDA;
 }
 
+// TMA map of the K codes as [page][64 slots][64 B] with `page_bytes` between
+// pages (4096 for the separate-tensor layout, 4352 when the scales follow the
+// codes inside each page); one box is one page.
+int encode_k_pages(CUtensorMap* map, void* base, uint64_t num_pages, uint64_t page_bytes) {
+  cuuint64_t dims[3] = {(cuuint64_t)kDimBytes, (cuuint64_t)kPage, (cuuint64_t)num_pages};
+  cuuint64_t strides[2] = {(cuuint64_t)kDimBytes, (cuuint64_t)page_bytes};
+  cuuint32_t box[3] = {(cuuint32_t)kDimBytes, (cuuint32_t)kPage, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? IDX_OK : IDX_ERR_CUDA;
+}
+
 struct Scratch {
   void* base = nullptr;
   ScratchLayout L{};
@@ -319,7 +340,25 @@ struct Call {
   const idx_tensor_t *out_phys, *out_raw;   // prefill outputs
   const idx_tensor_t *scores, *logits;      // dense / debug score outputs
   Path path;
+  const idx_tensor_t* k_pages = nullptr;    // page-interleaved K cache (replaces the two K tensors)
 };
+
+// Where the scorer finds a page's codes and scales for a call.
+struct KSource {
+  void* codes;
+  uint64_t page_bytes;
+  const uint8_t* scales;
+  int64_t scale_stride_words;
+};
+
+KSource k_source(const Call& c) {
+  if (c.k_pages)
+    return {c.k_pages->data, (uint64_t)kPage * (kDimBytes + kNumSF),
+            (const uint8_t*)c.k_pages->data + kPage * kDimBytes,
+            (int64_t)kPage * (kDimBytes + kNumSF) / 4};
+  return {c.k_cache_fp4->data, (uint64_t)kPage * kDimBytes, (const uint8_t*)c.k_scale->data,
+          (int64_t)kPage};
+}
 
 int read_status_and_free(const Scratch& s, cudaStream_t stream, uint32_t* status) {
   // pageable destination: returns once the copy (and all earlier work on the
@@ -350,9 +389,9 @@ int run(const Call& c, cudaStream_t stream) {
   }
   const idx_tensor_t* all[] = {c.q_fp4, c.q_scale, c.k_cache_fp4, c.k_scale, c.weights, c.page_table,
                                c.row_req, c.row_start, c.row_end, c.out_phys, c.out_raw,
-                               c.scores, c.logits};
+                               c.scores, c.logits, c.k_pages};
   int dev = -1;
-  int st = common_device(all, 13, &dev);
+  int st = common_device(all, 14, &dev);
   if (st) return st;
   DeviceGuard guard(dev);
   if (!guard.ok()) return IDX_ERR_CUDA;
@@ -366,7 +405,7 @@ int run(const Call& c, cudaStream_t stream) {
   if (prefill && !topk_supported(c.topk)) return fail(IDX_ERR_UNSUPPORTED);
   Sizes sz;
   st = check_inputs(c.q_fp4, c.q_scale, c.k_cache_fp4, c.k_scale, c.weights, c.page_table,
-                    c.row_req, c.row_start, c.row_end, &sz);
+                    c.row_req, c.row_start, c.row_end, &sz, c.k_pages);
   if (st) return fail(st);
   int64_t score_stride = 0, logits_stride = 0, check_end = 0;
   if (c.path != Path::kFused && c.scores) {
@@ -440,7 +479,8 @@ int run(const Call& c, cudaStream_t stream) {
   cuda_err |= launch_plan(pp, stream) != cudaSuccess;
 
   CUtensorMap tmap_k, tmap_q;
-  if (encode_2d_u8(&tmap_k, c.k_cache_fp4->data, (uint64_t)sz.num_pages * kPage, kPage) ||
+  const KSource ks = k_source(c);
+  if (encode_k_pages(&tmap_k, ks.codes, (uint64_t)sz.num_pages, ks.page_bytes) ||
       encode_2d_u8(&tmap_q, c.q_fp4->data, (uint64_t)sz.rows * kHeads, kRowsPerChunk * kHeads)) {
     uint32_t dummy;
     read_status_and_free(s, stream, &dummy);
@@ -448,7 +488,8 @@ int run(const Call& c, cudaStream_t stream) {
   }
   ScoreParams sp{};
   sp.q_scale = (const uint8_t*)c.q_scale->data;
-  sp.k_scale = (const uint8_t*)c.k_scale->data;
+  sp.k_scale = ks.scales;
+  sp.k_scale_stride = ks.scale_stride_words;
   sp.weights = (const float*)c.weights->data;
   sp.page_table = pp.page_table;
   sp.row_start = pp.row_start;
@@ -623,7 +664,8 @@ int run_fixed_scratch(const Call& c, cudaStream_t stream) {
   int cuda_err = launch_plan(pp, stream) != cudaSuccess;
 
   CUtensorMap tmap_k, tmap_q;
-  if (encode_2d_u8(&tmap_k, c.k_cache_fp4->data, (uint64_t)sz.num_pages * kPage, kPage) ||
+  const KSource ks = k_source(c);
+  if (encode_k_pages(&tmap_k, ks.codes, (uint64_t)sz.num_pages, ks.page_bytes) ||
       encode_2d_u8(&tmap_q, c.q_fp4->data, (uint64_t)sz.rows * kHeads, kRowsPerChunk * kHeads)) {
     cudaStreamSynchronize(stream);
     cudaGetLastError();
@@ -631,7 +673,8 @@ int run_fixed_scratch(const Call& c, cudaStream_t stream) {
   }
   ScoreParams sp{};
   sp.q_scale = (const uint8_t*)c.q_scale->data;
-  sp.k_scale = (const uint8_t*)c.k_scale->data;
+  sp.k_scale = ks.scales;
+  sp.k_scale_stride = ks.scale_stride_words;
   sp.weights = (const float*)c.weights->data;
   sp.page_table = pp.page_table;
   sp.row_start = pp.row_start;
@@ -768,12 +811,14 @@ int run_stream_ordered(const Call& c, void* workspace, uint64_t workspace_bytes,
   cuda_err |= launch_plan(pp, stream) != cudaSuccess;
 
   CUtensorMap tmap_k, tmap_q;
-  if (encode_2d_u8(&tmap_k, c.k_cache_fp4->data, (uint64_t)sz.num_pages * kPage, kPage) ||
+  const KSource ks = k_source(c);
+  if (encode_k_pages(&tmap_k, ks.codes, (uint64_t)sz.num_pages, ks.page_bytes) ||
       encode_2d_u8(&tmap_q, c.q_fp4->data, (uint64_t)sz.rows * kHeads, kRowsPerChunk * kHeads))
     return IDX_ERR_CUDA;
   ScoreParams sp{};
   sp.q_scale = (const uint8_t*)c.q_scale->data;
-  sp.k_scale = (const uint8_t*)c.k_scale->data;
+  sp.k_scale = ks.scales;
+  sp.k_scale_stride = ks.scale_stride_words;
   sp.weights = (const float*)c.weights->data;
   sp.page_table = pp.page_table;
   sp.row_start = pp.row_start;
@@ -858,6 +903,17 @@ int idx_topk_fp4_prefill_async(const idx_tensor_t* q_fp4, const idx_tensor_t* q_
   Call c{q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req, row_start, row_end,
          topk, out_phys_slot, out_raw_idx, nullptr, nullptr, Path::kFused};
   return run_stream_ordered(c, workspace, workspace_bytes, status, (cudaStream_t)stream);
+}
+
+int idx_topk_fp4_prefill_paged(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                               const idx_tensor_t* k_pages, const idx_tensor_t* weights,
+                               const idx_tensor_t* page_table, const idx_tensor_t* row_req,
+                               const idx_tensor_t* row_start, const idx_tensor_t* row_end,
+                               int32_t topk, const idx_tensor_t* out_phys_slot,
+                               const idx_tensor_t* out_raw_idx, idx_stream_t stream) {
+  Call c{q_fp4, q_scale, nullptr, nullptr, weights, page_table, row_req, row_start, row_end,
+         topk, out_phys_slot, out_raw_idx, nullptr, nullptr, Path::kFused, k_pages};
+  return run(c, (cudaStream_t)stream);
 }
 
 int idx_dense_topk_fp4_prefill(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,

@@ -127,7 +127,8 @@ enum ScoreMode : int32_t { kModeSelect = 0, kModeDense = 1 };
 // Parameters of the scoring kernel (tensor maps are separate launch arguments).
 struct ScoreParams {
   const uint8_t* q_scale;
-  const uint8_t* k_scale;
+  const uint8_t* k_scale;    // page p's 64 scale words start at word p * k_scale_stride
+  int64_t k_scale_stride;    // 32-bit words between consecutive pages' scales
   const float* weights;
   const int32_t* page_table;
   const int32_t* row_start;

@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmap_k);
       prefetch_tmap(&tmap_q);
     }
-    const uint32_t* kscale = reinterpret_cast<const uint32_t*>(p.k_scale);  // [page][slot] words
+    const uint32_t* kscale = reinterpret_cast<const uint32_t*>(p.k_scale);  // per page: 64 slot words
     uint32_t n_issued = 0;  // K tiles of the CTA's sequence so far (both producers)
     uint32_t q_issued[2] = {0, 0};
     bool ok = true;
@@ -431,10 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto load_scales = [&](int32_t pg0, int32_t pg1, uint32_t (&w)[4]) {
         const bool v0 = pg0 >= 0 && pg0 < p.num_pages, v1 = pg1 >= 0 && pg1 < p.num_pages;
-        w[0] = v0 ? kscale[(int64_t)pg0 * kPage + lane] : 0u;
-        w[1] = v0 ? kscale[(int64_t)pg0 * kPage + 32 + lane] : 0u;
-        w[2] = v1 ? kscale[(int64_t)pg1 * kPage + lane] : 0u;
-        w[3] = v1 ? kscale[(int64_t)pg1 * kPage + 32 + lane] : 0u;
+        w[0] = v0 ? kscale[(int64_t)pg0 * p.k_scale_stride + lane] : 0u;
+        w[1] = v0 ? kscale[(int64_t)pg0 * p.k_scale_stride + 32 + lane] : 0u;
+        w[2] = v1 ? kscale[(int64_t)pg1 * p.k_scale_stride + lane] : 0u;
+        w[3] = v1 ? kscale[(int64_t)pg1 * p.k_scale_stride + 32 + lane] : 0u;
       };
       uint32_t wnext[4] = {0u, 0u, 0u, 0u};
       bool have_next = false;
@@ -488,8 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (bytes) {
             mbar_arrive_expect_tx(fb, bytes);
             const uint32_t a = sbase + kOffA + st * kABytes;
-            if (v0) tma_load_2d(a, &tmap_k, 0, pg0 * kPage, fb);
-            if (v1) tma_load_2d(a + kPageBytes, &tmap_k, 0, pg1 * kPage, fb);
+            if (v0) tma_load_3d(a, &tmap_k, 0, 0, pg0, fb);
+            if (v1) tma_load_3d(a + kPageBytes, &tmap_k, 0, 0, pg1, fb);
           } else {
             mbar_arrive(fb);
           }

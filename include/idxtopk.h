@@ -117,6 +117,24 @@ int idx_topk_fp4_prefill(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
                          idx_stream_t stream);
 
 /*
+ * idx_topk_fp4_prefill for a page-interleaved K cache (a consumer layout named
+ * as follow-up work in "[FlyDSL][DSv4] Prototype FP4 MQA streaming TopK",
+ * ROCm/aiter#5282, Scope): each physical page holds its codes and then its
+ * scales, so one page is one contiguous 4352-byte record.
+ *   k_pages u8 [NP, 4352]   bytes [0, 4096): 64 slots x 64 B of E2M1 codes
+ *                           (as k_cache_fp4[page]); bytes [4096, 4352): 64
+ *                           slots x 4 UE8M0 scales (as k_scale[page]).
+ * Every other argument, the results and the error behaviour are those of
+ * idx_topk_fp4_prefill; the outputs are identical for the same data.
+ */
+int idx_topk_fp4_prefill_paged(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                               const idx_tensor_t* k_pages, const idx_tensor_t* weights,
+                               const idx_tensor_t* page_table, const idx_tensor_t* row_req,
+                               const idx_tensor_t* row_start, const idx_tensor_t* row_end,
+                               int32_t topk, const idx_tensor_t* out_phys_slot,
+                               const idx_tensor_t* out_raw_idx, idx_stream_t stream);
+
+/*
  * Stream-ordered variant of idx_topk_fp4_prefill for decode loops and CUDA
  * graphs: the same operation and outputs, with no allocation and no host
  * synchronisation, so a call may be captured into a graph and replayed.  The
