@@ -36,7 +36,7 @@ namespace idxk {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kStages = 8;       // K-tile ring (TMA latency x tile rate)
+constexpr int kStages = 6;       // K-tile ring (TMA latency x tile rate)
 constexpr int kEpiWarp0 = 4;
 constexpr int kProducer2 = 3;  // second TMA producer warp
 static_assert(kStages % 2 == 0, "producers own the stages of one parity each");
@@ -103,7 +103,7 @@ constexpr uint32_t kIdescK1 = idesc_mxf4(128, kAccCols, 2);
 // exactly topk keys over all four regions and each warp compacts its own
 // region in place.  A region never has to hold more than topk survivors plus
 // one check window of appends.
-constexpr int kCheckTiles = 8;
+constexpr int kCheckTiles = 12;
 // The candidate buffers take all shared memory the pipeline leaves free.
 constexpr uint32_t kMaxSmem = 227u * 1024u;
 constexpr uint32_t kCandCap = (kMaxSmem - 1024u - kOffCand) / (kRowsPerBlock * 8u) / 128u * 128u;
