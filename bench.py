@@ -372,6 +372,26 @@ def main():
                               "score_storage_bytes": ws.numel() * 4}
         del ws
 
+    if not args.no_dense:
+        # context-tiled comparison path: bounded fp32 chunks of 16384 positions
+        tile = 16384
+        t_phys = torch.empty_like(phys)
+        t_raw = torch.empty_like(raw)
+        t_ms = []
+        for i in range(2 + 5):
+            flush.zero_()
+            ev0.record()
+            m.idx_tiled_topk_fp4_prefill(**dev, topk=K, out_phys_slot=t_phys, out_raw_idx=t_raw,
+                                         context_tile=tile)
+            ev1.record()
+            ev1.synchronize()
+            if i >= 2:
+                t_ms.append(ev0.elapsed_time(ev1))
+        line["tiled_topk"] = {"ms_median": statistics.median(t_ms), "context_tile": tile,
+                              "chunk_buffer_bytes": R * tile * 4,
+                              "indices_identical": bool(torch.equal(t_raw, raw) and
+                                                        torch.equal(t_phys, phys))}
+
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(p, args.cpu_seconds)
     if rank == 0:

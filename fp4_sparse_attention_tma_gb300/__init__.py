@@ -21,7 +21,7 @@ from . import _lib
 
 __all__ = ["IdxError", "SUPPORTED_K", "idx_topk_fp4_prefill", "idx_topk_fp4_prefill_noalloc",
            "idx_topk_fp4_prefill_async", "idx_topk_fp4_prefill_paged",
-           "idx_dense_topk_fp4_prefill",
+           "idx_dense_topk_fp4_prefill", "idx_tiled_topk_fp4_prefill",
            "idx_fp4_debug_scores", "idx_topk_select_scores", "idx_topk_supported_k",
            "idx_topk_status_string", "idx_topk_fp4_scratch_bytes", "idx_topk_scratch_high_water",
            "dense_score_bytes", "STATUS", "idx_topk_set_timing",
@@ -137,6 +137,19 @@ def idx_dense_topk_fp4_prefill(q_fp4, q_scale, k_cache_fp4, k_scale, weights, pa
     code = lib.idx_dense_topk_fp4_prefill(*[_ref(d) for d in ds[:9]], int(topk), _ref(ds[9]),
                                           _ref(ds[10]), _ref(ds[11]), _stream(stream))
     return _check(code, "idx_dense_topk_fp4_prefill", raise_on_error)
+
+
+def idx_tiled_topk_fp4_prefill(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                               row_start, row_end, topk, out_phys_slot, out_raw_idx=None,
+                               context_tile=16384, stream=None, raise_on_error=True) -> int:
+    """Comparison path: score `context_tile` positions at a time into a bounded
+    fp32 buffer, fold each chunk into the rows' running TopK."""
+    lib = _lib.load()
+    ds = [_desc(t) for t in (q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                             row_start, row_end, out_phys_slot, out_raw_idx)]
+    code = lib.idx_tiled_topk_fp4_prefill(*[_ref(d) for d in ds[:9]], int(topk), int(context_tile),
+                                          _ref(ds[9]), _ref(ds[10]), _stream(stream))
+    return _check(code, "idx_tiled_topk_fp4_prefill", raise_on_error)
 
 
 def idx_fp4_debug_scores(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,

@@ -90,6 +90,9 @@ EXPORTS = {
     "idx_topk_fp4_prefill_noalloc": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
                                      [ctypes.c_int32, ctypes.POINTER(IdxTensor),
                                       ctypes.POINTER(IdxTensor), ctypes.c_void_p]),
+    "idx_tiled_topk_fp4_prefill": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
+                                   [ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(IdxTensor),
+                                    ctypes.POINTER(IdxTensor), ctypes.c_void_p]),
     "idx_dense_topk_fp4_prefill": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
                                    [ctypes.c_int32] + [ctypes.POINTER(IdxTensor)] * 3 +
                                    [ctypes.c_void_p]),

@@ -163,6 +163,130 @@ cudaError_t launch_finish(const FinishParams& p, cudaStream_t stream) {
 }
 
 namespace {
+// Windows of one context chunk [c0, c1): rows longer than topk keep the part
+// of their window inside the chunk; shorter rows (closed form) get none.
+__global__ void clip_windows_kernel(const int32_t* row_start, const int32_t* row_end, int32_t rows,
+                                    int32_t c0, int32_t c1, int32_t topk, int32_t* out_start,
+                                    int32_t* out_end) {
+  for (int32_t r = blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += gridDim.x * blockDim.x) {
+    const int32_t s0 = row_start[r], s1 = row_end[r];
+    int32_t a = s0 > c0 ? s0 : c0, b = s1 < c1 ? s1 : c1;
+    if ((int64_t)s1 - s0 <= topk || a > b) a = b = s0;
+    out_start[r] = a;
+    out_end[r] = b;
+  }
+}
+
+// One CTA per row: the row's running TopK (keys in run_keys, count run_cnt,
+// threshold run_tau) absorbs the chunk's materialised scores
+// (chunk[r * stride + s - c0] for s in the clipped window); after the last
+// chunk the keys are sorted and written like the merge of the fused path.
+template <int TOPK>
+__global__ void __launch_bounds__(kFinThreads) tile_merge_kernel(TileMergeParams p) {
+  __shared__ __align__(16) uint64_t buf[kFinCap];
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t bc[4];
+  __shared__ uint32_t cnt;
+  __shared__ uint64_t tau;
+  const int r = blockIdx.x;
+  const int tid = threadIdx.x;
+  if (read_status(p.hdr) != kOk) return;
+  const int32_t s0 = p.row_start[r], s1 = p.row_end[r];
+  const int64_t len = (int64_t)s1 - s0;
+  const int32_t* row_pt = p.page_table + (int64_t)p.row_req[r] * p.max_pages;
+  if (len <= TOPK) {
+    if (!p.last) return;
+    for (int i = tid; i < TOPK; i += kFinThreads) {
+      const int32_t raw = i < len ? s0 + i : -1;
+      if (p.out_raw) p.out_raw[(int64_t)r * TOPK + i] = raw;
+      p.out_phys[(int64_t)r * TOPK + i] = map_phys(row_pt, raw);
+    }
+    return;
+  }
+  uint64_t* run = p.run_keys + (int64_t)r * TOPK;
+  const uint32_t n_run = p.first ? 0u : p.run_cnt[r];
+  uint64_t t = p.first ? 0ull : p.run_tau[r];
+  for (uint32_t i = tid; i < n_run; i += kFinThreads) buf[i] = run[i];
+  if (tid == 0) {
+    cnt = n_run;
+    tau = t;
+  }
+  __syncthreads();
+  const int32_t a = s0 > p.c0 ? s0 : p.c0, b = s1 < p.c1 ? s1 : p.c1;
+  const float* src = p.chunk + (int64_t)r * p.stride - p.c0;
+  for (int64_t base = a; base < b; base += kFinBatch) {
+    bool over = false;
+#pragma unroll
+    for (int e = 0; e < kFinPer; ++e) {
+      const int64_t s = base + e * kFinThreads + tid;
+      const bool in = s < b;
+      const float v = in ? src[s] : 0.f;
+      const uint64_t key = order_key(v, (int32_t)s);
+      over |= sel_append(buf, &cnt, kFinCap, kFinCap - kFinBatch, in && key >= t, key);
+    }
+    if (bar_red_or(kFinBar, kFinThreads, over)) {
+      sel_compact<kFinThreads, kFinCap>(buf, &cnt, &tau, hist, bc, TOPK, tid, kFinBar, p.hdr);
+      t = *(volatile uint64_t*)&tau;
+    }
+  }
+  __syncthreads();
+  sel_compact<kFinThreads, kFinCap>(buf, &cnt, &tau, hist, bc, TOPK, tid, kFinBar, p.hdr);
+  const uint32_t n = min(*(volatile uint32_t*)&cnt, (uint32_t)TOPK);
+  if (!p.last) {
+    for (uint32_t i = tid; i < n; i += kFinThreads) run[i] = buf[i];
+    if (tid == 0) {
+      p.run_cnt[r] = n;
+      p.run_tau[r] = *(volatile uint64_t*)&tau;
+    }
+    return;
+  }
+  if (n < (uint32_t)TOPK) {
+    if (tid == 0) raise_status(p.hdr, kErrInternal, 401);
+    for (int i = n + tid; i < TOPK; i += kFinThreads) buf[i] = 0ull;
+  }
+  __syncthreads();
+  for (int size = 2; size <= TOPK; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < TOPK / 2; i += kFinThreads) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const uint64_t x = buf[lo], y = buf[hi];
+        const bool desc = (lo & size) == 0;
+        if (desc ? (x < y) : (x > y)) {
+          buf[lo] = y;
+          buf[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = tid; i < TOPK; i += kFinThreads) {
+    const uint64_t key = buf[i];
+    const int32_t raw = key != 0ull ? key_index(key) : -1;
+    if (p.out_raw) p.out_raw[(int64_t)r * TOPK + i] = raw;
+    p.out_phys[(int64_t)r * TOPK + i] = map_phys(row_pt, raw);
+  }
+}
+}  // namespace
+
+cudaError_t launch_clip_windows(const int32_t* row_start, const int32_t* row_end, int32_t rows,
+                                int32_t c0, int32_t c1, int32_t topk, int32_t* out_start,
+                                int32_t* out_end, cudaStream_t stream) {
+  const int grid = rows > 0 ? (rows + 255) / 256 : 1;
+  clip_windows_kernel<<<grid, 256, 0, stream>>>(row_start, row_end, rows, c0, c1, topk, out_start,
+                                                out_end);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tile_merge(const TileMergeParams& p, cudaStream_t stream) {
+  if (p.rows == 0) return cudaSuccess;
+  if (p.topk == 512) tile_merge_kernel<512><<<p.rows, kFinThreads, 0, stream>>>(p);
+  else if (p.topk == 1024) tile_merge_kernel<1024><<<p.rows, kFinThreads, 0, stream>>>(p);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+namespace {
 __global__ void publish_status_kernel(const PlanHeader* hdr, uint32_t* status_out,
                                       int32_t* out_phys, int32_t* out_raw, int64_t n) {
   const uint32_t st = read_status(hdr);

@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "idx_internal.h"
 #include "idx_launch.h"
@@ -720,6 +721,182 @@ int run_fixed_scratch(const Call& c, cudaStream_t stream) {
   return IDX_OK;
 }
 
+// ----------------------------------------- context-tiled comparison path ----
+//
+// Scores one context chunk of `tile` positions at a time into a bounded fp32
+// buffer [rows, tile] (the fused kernel's dense mode on the chunk's part of
+// each window) and folds every chunk into each row's running TopK; the
+// outputs are the fused path's.  Scratch: plan + rows * tile * 4 B + rows *
+// topk * 8 B, independent of the context length.
+int run_tiled(const Call& c, int32_t tile, cudaStream_t stream) {
+  Outputs outs;
+  int st = check_output(c.out_phys, c.q_fp4 ? c.q_fp4->shape[0] : 0, c.topk);
+  if (st) return st;
+  outs.t[0] = c.out_phys;
+  if (c.out_raw) {
+    if ((st = check_output(c.out_raw, c.q_fp4 ? c.q_fp4->shape[0] : 0, c.topk))) return st;
+    outs.t[1] = c.out_raw;
+  }
+  const idx_tensor_t* all[] = {c.q_fp4, c.q_scale, c.k_cache_fp4, c.k_scale, c.weights,
+                               c.page_table, c.row_req, c.row_start, c.row_end, c.out_phys,
+                               c.out_raw};
+  int dev = -1;
+  if ((st = common_device(all, 11, &dev))) return st;
+  DeviceGuard guard(dev);
+  if (!guard.ok()) return IDX_ERR_CUDA;
+  st = check_stream(stream, dev);
+  if (st == IDX_ERR_UNSUPPORTED) return st;
+  auto fail = [&](int code) {
+    fill_minus_one(outs, stream);
+    return code;
+  };
+  if (st) return fail(st);
+  if (!topk_supported(c.topk)) return fail(IDX_ERR_UNSUPPORTED);
+  if (tile < 1024 || tile % kTile != 0) return fail(IDX_ERR_INVALID_ARGUMENT);
+  Sizes sz;
+  if ((st = check_inputs(c.q_fp4, c.q_scale, c.k_cache_fp4, c.k_scale, c.weights, c.page_table,
+                         c.row_req, c.row_start, c.row_end, &sz)))
+    return fail(st);
+  if (sz.rows == 0) return IDX_OK;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(dev, &ds))) return fail(st);
+  if (!(ds->cc_major == 10 && ds->cc_minor == 3)) return fail(IDX_ERR_UNSUPPORTED);
+  const int grid = ds->sm_count;
+  const int64_t R = sz.rows;
+  Scratch s;
+  s.L = scratch_layout(R, c.topk, grid, false);
+  int64_t chunk_bytes, run_bytes;
+  if (!mul_ok(R, (int64_t)tile * 4, &chunk_bytes) || !mul_ok(R, (int64_t)c.topk * 8, &run_bytes))
+    return fail(IDX_ERR_OVERFLOW);
+  const size_t off_chunk = align_up(s.L.total, 256);
+  const size_t off_run = align_up(off_chunk + (size_t)chunk_bytes, 256);
+  const size_t off_cnt = align_up(off_run + (size_t)run_bytes, 256);
+  const size_t off_tau = align_up(off_cnt + (size_t)R * 4, 256);
+  const size_t off_win = align_up(off_tau + (size_t)R * 8, 256);
+  const size_t total = off_win + align_up((size_t)R * 8, 256);
+  if (cudaMallocFromPoolAsync(&s.base, total, ds->pool, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(IDX_ERR_CUDA);
+  }
+  cudaMemsetAsync(s.hdr(), 0, sizeof(PlanHeader), stream);
+  int32_t* cs = s.at<int32_t>(off_win);
+  int32_t* ce = cs + R;
+  int32_t max_end = 0;
+  {
+    // the chunk loop needs the largest window end; a short read of row_end
+    // (the call synchronises on the caller stream anyway)
+    std::vector<int32_t> ends((size_t)R);
+    if (cudaMemcpyAsync(ends.data(), c.row_end->data, (size_t)R * 4, cudaMemcpyDeviceToHost,
+                        stream) != cudaSuccess) {
+      cudaGetLastError();
+      uint32_t dummy;
+      read_status_and_free(s, stream, &dummy);
+      return fail(IDX_ERR_CUDA);
+    }
+    for (int32_t e : ends) max_end = e > max_end ? e : max_end;
+  }
+  if ((int64_t)max_end > sz.max_pages * kPage) {  // also bounds the chunk loop
+    uint32_t dummy;
+    read_status_and_free(s, stream, &dummy);
+    return fail(IDX_ERR_INVALID_METADATA);
+  }
+  CUtensorMap tmap_k, tmap_q;
+  const KSource ks = k_source(c);
+  if (encode_k_pages(&tmap_k, ks.codes, (uint64_t)sz.num_pages, ks.page_bytes) ||
+      encode_2d_u8(&tmap_q, c.q_fp4->data, (uint64_t)R * kHeads, kRowsPerChunk * kHeads)) {
+    uint32_t dummy;
+    read_status_and_free(s, stream, &dummy);
+    return fail(IDX_ERR_CUDA);
+  }
+  int cuda_err = 0;
+  CallTimer timer;
+  timer.mark(0, stream);
+  const int32_t n_chunks = max_end > 0 ? (max_end + tile - 1) / tile : 1;
+  for (int32_t k = 0; k < n_chunks; ++k) {
+    const int32_t c0 = k * tile, c1 = c0 + tile;
+    cuda_err |= launch_clip_windows((const int32_t*)c.row_start->data,
+                                    (const int32_t*)c.row_end->data, (int32_t)R, c0, c1, c.topk,
+                                    cs, ce, stream) != cudaSuccess;
+    PlanParams pp{};
+    pp.row_req = (const int32_t*)c.row_req->data;
+    pp.row_start = cs;
+    pp.row_end = ce;
+    pp.page_table = (const int32_t*)c.page_table->data;
+    pp.rows = (int32_t)R;
+    pp.num_req = (int32_t)sz.num_req;
+    pp.max_pages = (int32_t)sz.max_pages;
+    pp.num_pages = (int32_t)sz.num_pages;
+    pp.score_thr = 0;
+    pp.grid = grid;
+    pp.check_end_le = -1;
+    pp.max_units = s.L.max_units;
+    pp.max_row_slots = s.L.max_row_slots;
+    pp.hdr = s.hdr();
+    pp.row_block = s.at<int32_t>(s.L.row_block);
+    pp.blocks = s.at<BlockInfo>(s.L.blocks);
+    pp.units = s.at<UnitInfo>(s.L.units);
+    pp.sched = s.at<int32_t>(s.L.sched);
+    cuda_err |= launch_plan(pp, stream) != cudaSuccess;
+    ScoreParams sp{};
+    sp.q_scale = (const uint8_t*)c.q_scale->data;
+    sp.k_scale = ks.scales;
+    sp.k_scale_stride = ks.scale_stride_words;
+    sp.weights = (const float*)c.weights->data;
+    sp.page_table = pp.page_table;
+    sp.row_start = cs;
+    sp.row_end = ce;
+    sp.rows = pp.rows;
+    sp.max_pages = pp.max_pages;
+    sp.num_pages = pp.num_pages;
+    sp.topk = 0;
+    sp.mode = kModeDense;
+    sp.score_thr = 0;
+    sp.hdr = pp.hdr;
+    sp.blocks = pp.blocks;
+    sp.units = pp.units;
+    sp.sched = pp.sched;
+    sp.dense_out = s.at<float>(off_chunk);
+    sp.dense_stride = tile;
+    sp.dense_col0 = c0;
+    cuda_err |= launch_score(tmap_k, tmap_q, sp, grid, stream) != cudaSuccess;
+    TileMergeParams mp{};
+    mp.row_req = pp.row_req;
+    mp.row_start = (const int32_t*)c.row_start->data;
+    mp.row_end = (const int32_t*)c.row_end->data;
+    mp.page_table = pp.page_table;
+    mp.rows = (int32_t)R;
+    mp.max_pages = pp.max_pages;
+    mp.topk = c.topk;
+    mp.c0 = c0;
+    mp.c1 = c1;
+    mp.first = k == 0;
+    mp.last = k == n_chunks - 1;
+    mp.stride = tile;
+    mp.chunk = sp.dense_out;
+    mp.run_keys = s.at<uint64_t>(off_run);
+    mp.run_cnt = s.at<uint32_t>(off_cnt);
+    mp.run_tau = s.at<uint64_t>(off_tau);
+    mp.hdr = pp.hdr;
+    mp.out_phys = (int32_t*)c.out_phys->data;
+    mp.out_raw = c.out_raw ? (int32_t*)c.out_raw->data : nullptr;
+    cuda_err |= launch_tile_merge(mp, stream) != cudaSuccess;
+  }
+  timer.mark(1, stream);
+  timer.mark(2, stream);
+  timer.mark(3, stream);
+  cudaEvent_t end_ev = nullptr;
+  if (timer.on && cudaEventCreate(&end_ev) == cudaSuccess) cudaEventRecord(end_ev, stream);
+  uint32_t status = 0;
+  st = read_status_and_free(s, stream, &status);
+  if (end_ev) {
+    timer.collect(end_ev);
+    cudaEventDestroy(end_ev);
+  }
+  if (cuda_err || st || cudaGetLastError() != cudaSuccess) return fail(IDX_ERR_CUDA);
+  if (status != kOk) return fail((int)status);
+  return IDX_OK;
+}
+
 // ------------------------------------------------ stream-ordered call ----
 //
 // The fused path with a caller workspace and a device status word: no
@@ -914,6 +1091,18 @@ int idx_topk_fp4_prefill_paged(const idx_tensor_t* q_fp4, const idx_tensor_t* q_
   Call c{q_fp4, q_scale, nullptr, nullptr, weights, page_table, row_req, row_start, row_end,
          topk, out_phys_slot, out_raw_idx, nullptr, nullptr, Path::kFused, k_pages};
   return run(c, (cudaStream_t)stream);
+}
+
+int idx_tiled_topk_fp4_prefill(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                               const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
+                               const idx_tensor_t* weights, const idx_tensor_t* page_table,
+                               const idx_tensor_t* row_req, const idx_tensor_t* row_start,
+                               const idx_tensor_t* row_end, int32_t topk, int32_t context_tile,
+                               const idx_tensor_t* out_phys_slot, const idx_tensor_t* out_raw_idx,
+                               idx_stream_t stream) {
+  Call c{q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req, row_start, row_end,
+         topk, out_phys_slot, out_raw_idx, nullptr, nullptr, Path::kFused};
+  return run_tiled(c, context_tile, (cudaStream_t)stream);
 }
 
 int idx_dense_topk_fp4_prefill(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,

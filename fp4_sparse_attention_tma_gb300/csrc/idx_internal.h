@@ -141,10 +141,28 @@ struct ScoreParams {
   const int32_t* sched;
   uint32_t* cand_cnt;
   uint64_t* cand_keys;
-  float* dense_out;        // [rows, dense_stride]
+  float* dense_out;        // [rows, dense_stride]; column = slot - dense_col0
   int64_t dense_stride;
+  int64_t dense_col0;
   float* logits_out;       // [rows, 64, logits_stride] or null
   int64_t logits_stride;
+};
+
+// Parameters of the context-tiled comparison path's per-chunk merge.
+struct TileMergeParams {
+  const int32_t* row_req;
+  const int32_t* row_start;   // the full windows
+  const int32_t* row_end;
+  const int32_t* page_table;
+  int32_t rows, max_pages, topk, c0, c1, first, last, pad;
+  int64_t stride;             // floats per row of the chunk buffer
+  const float* chunk;         // [rows, stride], column = slot - c0
+  uint64_t* run_keys;         // [rows, topk] running candidates
+  uint32_t* run_cnt;          // [rows]
+  uint64_t* run_tau;          // [rows] running threshold
+  PlanHeader* hdr;
+  int32_t* out_phys;
+  int32_t* out_raw;           // nullable
 };
 
 // Parameters of the row finishing kernels (merge of unit candidates, or TopK of

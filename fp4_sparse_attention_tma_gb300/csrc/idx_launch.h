@@ -41,6 +41,13 @@ cudaError_t launch_finish(const FinishParams& p, cudaStream_t stream);
 cudaError_t launch_validate_windows(const int32_t* row_start, const int32_t* row_end, int32_t rows,
                                     int64_t width, PlanHeader* hdr, cudaStream_t stream);
 
+// Context-tiled comparison path: windows of one chunk, and the per-chunk
+// merge into each row's running TopK (writing the outputs after the last).
+cudaError_t launch_clip_windows(const int32_t* row_start, const int32_t* row_end, int32_t rows,
+                                int32_t c0, int32_t c1, int32_t topk, int32_t* out_start,
+                                int32_t* out_end, cudaStream_t stream);
+cudaError_t launch_tile_merge(const TileMergeParams& p, cudaStream_t stream);
+
 // Stream-ordered end of a call whose status is not read by the host: copies
 // the status word to `status_out` and, when it is not kOk, fills the n
 // entries of out_phys (and out_raw, when given) with -1.

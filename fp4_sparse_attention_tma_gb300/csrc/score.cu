@@ -656,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           auto tail = [&]() {
             const float sc = head_sum_final(pacc);
             if constexpr (MODE == kModeDense) {
-              if (pwin) p.dense_out[row * p.dense_stride + pslot] = sc;
+              if (pwin) p.dense_out[row * p.dense_stride + (pslot - p.dense_col0)] = sc;
             } else {
               // cheap 32-bit test first; the low word only decides exact ties
               const uint32_t k32 = score_key(sc);

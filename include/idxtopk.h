@@ -234,6 +234,26 @@ int idx_topk_set_timing(int32_t enable);
 int idx_topk_last_timings(float* ms4);
 
 /*
+ * Context-tiled comparison path (an ablation of the fused design: "[FlyDSL]
+ * [DSv4] Prototype FP4 MQA streaming TopK", ROCm/aiter#5282, Changes, names a
+ * bounded context-tiled fallback).  The same operation and outputs as
+ * idx_topk_fp4_prefill, computed by scoring `context_tile` logical positions
+ * at a time into a materialised fp32 buffer [rows, context_tile] and folding
+ * each chunk into every row's running TopK.  Scratch is bounded by rows *
+ * (context_tile * 4 + topk * 8) bytes plus the plan, not by the context.
+ *   context_tile  positions per chunk, a multiple of 128 and >= 1024.
+ * Errors and ownership as idx_topk_fp4_prefill (a bad context_tile returns
+ * IDX_ERR_INVALID_ARGUMENT).
+ */
+int idx_tiled_topk_fp4_prefill(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                               const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
+                               const idx_tensor_t* weights, const idx_tensor_t* page_table,
+                               const idx_tensor_t* row_req, const idx_tensor_t* row_start,
+                               const idx_tensor_t* row_end, int32_t topk, int32_t context_tile,
+                               const idx_tensor_t* out_phys_slot, const idx_tensor_t* out_raw_idx,
+                               idx_stream_t stream);
+
+/*
  * Debug / dense scorer: the same scoring kernel as the fused path, writing the
  * fp32 scores instead of selecting.
  *   out_scores f32 [R, S]      score[r, s] written for every s in [start_r, end_r)
