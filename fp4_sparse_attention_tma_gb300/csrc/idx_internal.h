@@ -23,9 +23,9 @@ constexpr int kNumSF = 4;           // D / 32 UE8M0 scales per row
 constexpr int kPage = 64;           // slots per KV page
 constexpr int kTile = 128;          // slots per K tile = MMA M
 constexpr int kRowsPerBlock = 3;    // query rows sharing one K tile (one per epilogue warpgroup)
-constexpr int kRowsPerChunk = 1;    // rows per TMEM accumulator (N = 64 heads)
+constexpr int kRowsPerChunk = 1;    // query rows per TMA box of the query block (64 head rows)
 constexpr int kChunks = kRowsPerBlock / kRowsPerChunk;
-constexpr int kAccStages = 2;       // TMEM accumulators per row (double buffer)
+constexpr int kAccStages = 2;       // TMEM accumulator buffers (double buffer, N = 3 x 64 each)
 constexpr int kMinUnitTiles = 32;   // shortest work unit (tiles), except whole short blocks
 constexpr int kUnitsPerCta = 4;     // target work units per persistent CTA
 

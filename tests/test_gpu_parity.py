@@ -129,7 +129,7 @@ def test_short_empty_and_boundary_rows():
 
 
 def test_many_requests_ragged_blocks():
-    # request boundaries that do not align with the 6-row blocks
+    # request boundaries that do not align with the 3-row blocks
     rng = np.random.default_rng(3)
     lens = [int(x) for x in rng.integers(600, 5000, size=9)]
     rows = [int(x) for x in rng.integers(1, 9, size=9)]
