@@ -10,6 +10,7 @@
 #include <climits>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -35,7 +36,7 @@ DeviceState g_dev[kMaxDevices];
 
 // Optional per-kernel timing of the last call (CUDA events on the caller's
 // stream around each launch): plan+page check, scorer, finish, whole call.
-bool g_timing = false;
+std::atomic<bool> g_timing{false};
 thread_local float g_last_ms[4] = {0.f, 0.f, 0.f, 0.f};
 
 struct CallTimer {
@@ -557,6 +558,9 @@ int run(const Call& c, cudaStream_t stream) {
 // first call that uses the device, with that device current.
 static __device__ __align__(256) unsigned char g_fixed_scratch[IDX_NOALLOC_SCRATCH_BYTES];
 void* g_fixed_ptr[kMaxDevices] = {};
+// held for the whole of a call that uses a device's buffer: concurrent calls
+// from several host threads run one after another instead of sharing it
+std::mutex g_fixed_call_mu[kMaxDevices];
 
 int fixed_scratch(int dev, void** out) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -630,6 +634,7 @@ int run_fixed_scratch(const Call& c, cudaStream_t stream) {
                     c.row_req, c.row_start, c.row_end, &sz);
   if (st) return fail(st);
   if (sz.rows == 0) return IDX_OK;
+  std::lock_guard<std::mutex> call_lock(g_fixed_call_mu[dev]);
   int sm = 0, major = 0, minor = 0;
   if ((st = device_info_no_pool(dev, &sm, &major, &minor))) return fail(st);
   if (!(major == 10 && minor == 3)) return fail(IDX_ERR_UNSUPPORTED);

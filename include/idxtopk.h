@@ -191,11 +191,11 @@ int idx_topk_fp4_prefill_async(const idx_tensor_t* q_fp4, const idx_tensor_t* q_
  *  - The first call on a device looks up the buffer's address there (the
  *    device is made current for it); make that first call before any stream
  *    capture begins.
- *  - All calls on one device share the one buffer: calls that overlap in time
- *    on that device (other streams, other host threads) race on it and give
- *    undefined results.  Serialise them.
- *  - The call returns after its work on `stream` has completed, like the
- *    allocating entry point, so back-to-back calls from one thread are safe.
+ *  - All calls on one device share the one buffer.  The call returns only
+ *    after its work on `stream` has completed, and a per-device lock held for
+ *    the whole call makes concurrent calls from several host threads run one
+ *    after another, so calls never overlap on the buffer (other streams of
+ *    the same process included; each process has its own buffer).
  */
 #define IDX_NOALLOC_SCRATCH_BYTES (48u * 1024u * 1024u)
 int idx_topk_fp4_prefill_noalloc(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,

@@ -1,7 +1,8 @@
 """The allocation-free entry point (scratch in the library's fixed per-device
 buffer) against the allocating one: two calls in a row on different problems
 give bit-identical outputs, and a problem larger than the fixed buffer is
-refused with IDX_ERR_SCRATCH_LIMIT and -1 outputs."""
+refused with IDX_ERR_SCRATCH_LIMIT and -1 outputs, and concurrent calls from
+several host threads each get their own correct result."""
 import numpy as np
 import pytest
 
@@ -72,3 +73,48 @@ def test_noalloc_refuses_problem_beyond_buffer():
     torch.cuda.synchronize()
     assert code == SCRATCH_LIMIT
     assert (phys.cpu().numpy() == -1).all() and (raw.cpu().numpy() == -1).all()
+
+
+def test_noalloc_concurrent_host_threads():
+    # several host threads, each on its own stream and problem, call the
+    # allocation-free entry at once: the per-device lock keeps them off each
+    # other's scratch, so every result equals the allocating call's
+    import threading
+    import torch
+    import fp4_sparse_attention_tma_gb300 as m
+    probs = [inputs.small_problem(seed=40 + i, topk=(512, 1024)[i % 2]) for i in range(4)]
+    devs = [H.to_device(p) for p in probs]
+    want = []
+    for p, d in zip(probs, devs):
+        code, _, raw_ref = H.run_fused(p, d)
+        assert code == 0
+        want.append(raw_ref)
+    got = [[] for _ in probs]
+    errors = []
+
+    def worker(i):
+        try:
+            p, d = probs[i], devs[i]
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(3):
+                    raw = torch.full((p.rows, p.topk), 7, dtype=torch.int32, device="cuda")
+                    phys = torch.full((p.rows, p.topk), 7, dtype=torch.int32, device="cuda")
+                    code = m.idx_topk_fp4_prefill_noalloc(**d, topk=p.topk, out_phys_slot=phys,
+                                                          out_raw_idx=raw, raise_on_error=False)
+                    s.synchronize()
+                    got[i].append((code, raw.cpu().numpy()))
+        except Exception as e:  # reported by the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(probs))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i in range(len(probs)):
+        assert len(got[i]) == 3
+        for code, raw in got[i]:
+            assert code == 0
+            np.testing.assert_array_equal(raw, want[i])
