@@ -208,7 +208,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   const int64_t n_units = s_unit_carry;
   if (read_status(hdr) != kOk) return;
 
-  // 5. schedule: longest units first (static round-robin over persistent CTAs)
+  // 5. schedule: longest units first (the scorer deals them to its persistent
+  //    CTAs band by band, alternating the direction)
   if (n_units <= kSortMax) {
     int64_t n2 = 1;
     while (n2 < n_units) n2 <<= 1;

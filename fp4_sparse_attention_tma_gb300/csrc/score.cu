@@ -298,6 +298,15 @@ struct UnitView {
   BlockInfo b;
 };
 
+// Schedule position of this CTA's i-th unit.  The units are sorted longest
+// first; band i (positions i*G .. i*G+G-1) is dealt to the CTAs in ascending
+// order when i is even and descending when odd, so a CTA that drew a longer
+// unit of one band draws a shorter one of the next.
+__device__ __forceinline__ int cta_unit(int i) {
+  const int c = (i & 1) ? (int)(gridDim.x - 1u - blockIdx.x) : (int)blockIdx.x;
+  return i * (int)gridDim.x + c;
+}
+
 __device__ __forceinline__ UnitView load_unit(const ScoreParams& p, int ui) {
   UnitView v;
   v.u = p.units[p.sched[ui]];
@@ -370,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t q_issued[2] = {0, 0};
     bool ok = true;
     for (int i = 0; ok; ++i) {
-      const int ui = blockIdx.x + i * gridDim.x;
+      const int ui = cta_unit(i);
       if (ui >= n_units) break;
       const UnitView uv = load_unit(p, ui);
       const int qb = i & 1;
@@ -519,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t b_desc0 = desc_kmajor_sw64(sbase + kOffB);
     bool ok = true;
     for (int i = 0; ok; ++i) {
-      const int ui = blockIdx.x + i * gridDim.x;
+      const int ui = cta_unit(i);
       if (ui >= n_units) break;
       const UnitInfo u = p.units[p.sched[ui]];
       const int qb = i & 1;
@@ -596,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_use = 0;
     bool ok = true;
     for (int i = 0; ok; ++i) {
-      const int ui = blockIdx.x + i * gridDim.x;
+      const int ui = cta_unit(i);
       if (ui >= n_units) break;
       const UnitView uv = load_unit(p, ui);
       const int qb = i & 1;
