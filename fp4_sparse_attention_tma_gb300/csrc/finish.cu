@@ -23,6 +23,7 @@ constexpr int kFinCap = 4096;
 constexpr int kFinPer = 4;  // keys per thread per batch
 constexpr int kFinBatch = kFinThreads * kFinPer;
 constexpr uint32_t kFinBar = 1;
+constexpr int kFinGridCap = 2048;  // CTAs of finish_kernel (rows strided over them)
 
 __device__ __forceinline__ int32_t map_phys(const int32_t* row_pt, int32_t raw) {
   if (raw < 0 || row_pt == nullptr) return -1;
@@ -30,16 +31,246 @@ __device__ __forceinline__ int32_t map_phys(const int32_t* row_pt, int32_t raw) 
   return (int32_t)v;
 }
 
+// One bitonic step at distance S (< E) between a thread's own keys t*E + e.
+template <int E, int S>
+__device__ __forceinline__ void sort_in_thread(uint64_t (&v)[E], int g0, int size) {
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    if ((e & S) != 0) continue;
+    const bool desc = ((g0 + e) & size) == 0;
+    const uint64_t a = v[e], b = v[e | S];
+    const bool sw = desc ? (a < b) : (a > b);
+    v[e] = sw ? b : a;
+    v[e | S] = sw ? a : b;
+  }
+}
+
+// Sorts the row's TOPK keys buf[0, TOPK) descending (score desc, then index
+// asc: a bitonic network) and writes the row's outputs.  Thread t holds the E
+// consecutive keys t*E .. t*E+E-1 in registers: exchanges at distances below E
+// stay in the thread, distances below 32*E go between the lanes of a warp,
+// and only the larger ones pass through shared memory.  The caller has filled
+// buf[0, TOPK) (zero keys pad an underfilled row) before a barrier.
+template <int TOPK>
+__device__ __forceinline__ void sort_emit(uint64_t* buf, int tid, const int32_t* row_pt,
+                                          int32_t* out_raw, int32_t* out_phys) {
+  constexpr int E = TOPK / kFinThreads;
+  static_assert(E == 2 || E == 4, "keys per thread");
+  const int g0 = tid * E;
+  uint64_t v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = buf[g0 + e];
+#pragma unroll 1
+  for (int size = 2; size <= TOPK; size <<= 1) {
+#pragma unroll 1
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride < E) {
+        if (stride == 1) {
+          sort_in_thread<E, 1>(v, g0, size);
+        } else if constexpr (E == 4) {
+          sort_in_thread<E, 2>(v, g0, size);
+        }
+      } else {
+        // the pair's lower position keeps the larger key in a descending
+        // block, the smaller one in an ascending block; all E keys of a
+        // thread share both properties at these distances
+        const bool keep_max = ((g0 & stride) == 0) == ((g0 & size) == 0);
+        if (stride < 32 * E) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const uint64_t o = __shfl_xor_sync(0xffffffffu, v[e], stride / E);
+            v[e] = keep_max ? (v[e] > o ? v[e] : o) : (v[e] < o ? v[e] : o);
+          }
+        } else {
+          __syncthreads();  // earlier readers of buf are done
+#pragma unroll
+          for (int e = 0; e < E; ++e) buf[g0 + e] = v[e];
+          __syncthreads();
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const uint64_t o = buf[(g0 + e) ^ stride];
+            v[e] = keep_max ? (v[e] > o ? v[e] : o) : (v[e] < o ? v[e] : o);
+          }
+        }
+      }
+    }
+  }
+  int32_t raw[E], phys[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    raw[e] = v[e] != 0ull ? key_index(v[e]) : -1;
+    phys[e] = map_phys(row_pt, raw[e]);
+  }
+  // E consecutive outputs per thread; rows start at multiples of 2 KB of a
+  // 16-byte aligned base
+  if constexpr (E == 4) {
+    if (out_raw) *reinterpret_cast<int4*>(out_raw + g0) = make_int4(raw[0], raw[1], raw[2], raw[3]);
+    if (out_phys)
+      *reinterpret_cast<int4*>(out_phys + g0) = make_int4(phys[0], phys[1], phys[2], phys[3]);
+  } else {
+    if (out_raw) *reinterpret_cast<int2*>(out_raw + g0) = make_int2(raw[0], raw[1]);
+    if (out_phys) *reinterpret_cast<int2*>(out_phys + g0) = make_int2(phys[0], phys[1]);
+  }
+}
+
+// A row whose block ran as a single work unit has at most TOPK candidates, all
+// of them the row's TopK, so it needs only the sort.  A team of TOPK / 512
+// warps per row holds the keys in registers (16 per lane: key
+// g = 512 * warp + 16 * lane + e of the sorting network in register e) and
+// runs the bitonic network: distances below 16 within a lane, below 512
+// between the lanes of a warp, 512 (TOPK = 1024 only) through shared memory
+// between the team's two warps.  The teams also handle every short row
+// (length <= TOPK: start .. end-1, then -1).  Rows of multi-unit blocks are
+// left to finish_kernel.
+constexpr int kTeamThreads = 256;
+constexpr int kTeamE = 16;          // keys per lane
+constexpr int kTeamKeys = 32 * kTeamE;
+
+// One bitonic step at distance S < kTeamE: between registers of the same lane.
+template <int S>
+__device__ __forceinline__ void team_reg_step(uint64_t (&v)[kTeamE], int g0, int size) {
+#pragma unroll
+  for (int e = 0; e < kTeamE; ++e) {
+    if ((e & S) != 0) continue;
+    const bool desc = ((g0 + e) & size) == 0;
+    const uint64_t a = v[e], b = v[e | S];
+    const bool sw = desc ? (a < b) : (a > b);
+    v[e] = sw ? b : a;
+    v[e | S] = sw ? a : b;
+  }
+}
+
+// keep the larger (or smaller) of each register and its partner's
+__device__ __forceinline__ uint64_t keep_of(uint64_t x, uint64_t o, bool keep_max) {
+  return keep_max ? (x > o ? x : o) : (x < o ? x : o);
+}
+
+// The network over N keys.  The loops over block sizes and distances stay
+// rolled (only the per-register work is unrolled) so that the code fits the
+// instruction cache.  xbuf: the team's 2 x 512-key exchange area (N = 1024).
+template <int N>
+__device__ __forceinline__ void team_sort(uint64_t (&v)[kTeamE], int g0, int lane,
+                                          uint64_t* xbuf, uint32_t bar_id) {
+#pragma unroll 1
+  for (int size = 2; size <= N; size <<= 1) {
+    int stride = size >> 1;
+    if (stride >= kTeamKeys) {  // the two warps' halves: size == N == 1024
+      const int w = g0 / kTeamKeys;
+#pragma unroll
+      for (int e = 0; e < kTeamE; ++e) xbuf[w * kTeamKeys + e * 32 + lane] = v[e];
+      bar_sync(bar_id, 64);
+      const bool keep_max = w == 0;  // descending block: the lower half keeps the larger
+#pragma unroll
+      for (int e = 0; e < kTeamE; ++e)
+        v[e] = keep_of(v[e], xbuf[(1 - w) * kTeamKeys + e * 32 + lane], keep_max);
+      stride >>= 1;
+    }
+#pragma unroll 1
+    for (; stride >= kTeamE; stride >>= 1) {
+      // distance >= kTeamE: between lanes; all registers of a lane keep the
+      // same side of their pairs
+      const bool keep_max = ((g0 & stride) == 0) == ((g0 & size) == 0);
+      const int lx = stride / kTeamE;
+#pragma unroll
+      for (int e = 0; e < kTeamE; ++e)
+        v[e] = keep_of(v[e], __shfl_xor_sync(0xffffffffu, v[e], lx), keep_max);
+    }
+#pragma unroll 1
+    for (; stride > 0; stride >>= 1) {
+      switch (stride) {
+        case 1: team_reg_step<1>(v, g0, size); break;
+        case 2: team_reg_step<2>(v, g0, size); break;
+        case 4: team_reg_step<4>(v, g0, size); break;
+        default: team_reg_step<8>(v, g0, size); break;
+      }
+    }
+  }
+}
+
+template <int TOPK>
+__global__ void __launch_bounds__(kTeamThreads) finish_rows_team_kernel(FinishParams p) {
+  constexpr int W = TOPK / kTeamKeys;  // warps per row
+  constexpr int kTeams = kTeamThreads / 32 / W;
+  __shared__ __align__(16) uint64_t xbuf[W == 2 ? kTeams * TOPK : 1];
+  __shared__ uint32_t team_ok[kTeams];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int team = warp / W, tw = warp % W;
+  const uint32_t bar_id = 1u + (uint32_t)team;
+  const int64_t r = (int64_t)blockIdx.x * kTeams + team;
+  if (r >= p.rows) return;  // the same for both warps of a team
+  // one status read per team, so that its warps take the same path
+  if (tw == 0 && lane == 0) team_ok[team] = read_status(p.hdr) == kOk;
+  if constexpr (W == 2) bar_sync(bar_id, 64);
+  else __syncwarp();
+  if (!((volatile uint32_t*)team_ok)[team]) return;
+  const int32_t s0 = p.row_start[r], s1 = p.row_end[r];
+  const int64_t len = (int64_t)s1 - s0;
+  const int32_t* row_pt =
+      p.page_table ? p.page_table + (int64_t)p.row_req[r] * p.max_pages : nullptr;
+  int32_t* out_raw = p.out_raw ? p.out_raw + r * TOPK : nullptr;
+  int32_t* out_phys = p.out_phys ? p.out_phys + r * TOPK : nullptr;
+  const int t = tw * 32 + lane;  // thread within the team
+  if (len <= TOPK) {
+    for (int i = t; i < TOPK; i += 32 * W) {
+      const int32_t raw = i < len ? s0 + i : -1;
+      if (out_raw) out_raw[i] = raw;
+      if (out_phys) out_phys[i] = map_phys(row_pt, raw);
+    }
+    return;
+  }
+  const BlockInfo bi = p.blocks[p.row_block[r]];
+  if (bi.n_units != 1) return;
+  const int64_t slot = bi.slot0 + (r - bi.row0);
+  const uint32_t n = min(p.cand_cnt[slot], (uint32_t)TOPK);
+  const uint64_t* keys = p.cand_keys + slot * TOPK;
+  uint64_t v[kTeamE];
+#pragma unroll
+  for (int e = 0; e < kTeamE; ++e) {
+    // any placement of the inputs suits the network: read coalesced; an
+    // underfilled row (never expected) is padded with the empty key 0, which
+    // maps to -1
+    const uint32_t i = (uint32_t)(tw * kTeamKeys + e * 32 + lane);
+    v[e] = i < n ? keys[i] : 0ull;
+  }
+  const int g0 = tw * kTeamKeys + lane * kTeamE;
+  team_sort<TOPK>(v, g0, lane, xbuf + (W == 2 ? team * TOPK : 0), bar_id);
+  // the lane now holds ranks g0 .. g0 + 15; rows start at multiples of 2 KB
+  // of a 16-byte aligned base
+#pragma unroll
+  for (int e = 0; e < kTeamE; e += 4) {
+    int32_t raw[4], phys[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      raw[k] = v[e + k] != 0ull ? key_index(v[e + k]) : -1;
+      phys[k] = map_phys(row_pt, raw[k]);
+    }
+    if (out_raw)
+      *reinterpret_cast<int4*>(out_raw + g0 + e) = make_int4(raw[0], raw[1], raw[2], raw[3]);
+    if (out_phys)
+      *reinterpret_cast<int4*>(out_phys + g0 + e) = make_int4(phys[0], phys[1], phys[2], phys[3]);
+  }
+}
+
+// Shared memory of a finishing CTA.
+struct FinSmem {
+  uint64_t buf[kFinCap];
+  uint32_t hist[256];
+  uint32_t bc[4];
+  uint32_t cnt;
+  uint32_t ok;
+  uint64_t tau;
+};
+
+// One row, by the whole CTA (every early return is uniform over the CTA).
 template <int TOPK, bool DENSE>
-__global__ void __launch_bounds__(kFinThreads) finish_kernel(FinishParams p) {
-  __shared__ __align__(16) uint64_t buf[kFinCap];
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t bc[4];
-  __shared__ uint32_t cnt;
-  __shared__ uint64_t tau;
-  const int r = blockIdx.x;
+__device__ __forceinline__ void finish_row(const FinishParams& p, int64_t r, FinSmem& sm) {
+  uint64_t* buf = sm.buf;
+  uint32_t* hist = sm.hist;
+  uint32_t* bc = sm.bc;
+  uint32_t& cnt = sm.cnt;
+  uint64_t& tau = sm.tau;
   const int tid = threadIdx.x;
-  if (read_status(p.hdr) != kOk) return;
   const int32_t s0 = p.row_start[r], s1 = p.row_end[r];
   const int64_t len = (int64_t)s1 - s0;
   const int32_t* row_pt =
@@ -48,12 +279,17 @@ __global__ void __launch_bounds__(kFinThreads) finish_kernel(FinishParams p) {
   int32_t* out_phys = p.out_phys ? p.out_phys + (int64_t)r * TOPK : nullptr;
 
   if (len <= TOPK) {
-    for (int i = tid; i < TOPK; i += kFinThreads) {
-      const int32_t raw = i < len ? s0 + i : -1;
-      if (out_raw) out_raw[i] = raw;
-      if (out_phys) out_phys[i] = map_phys(row_pt, raw);
+    if constexpr (DENSE) {
+      for (int i = tid; i < TOPK; i += kFinThreads) {
+        const int32_t raw = i < len ? s0 + i : -1;
+        if (out_raw) out_raw[i] = raw;
+        if (out_phys) out_phys[i] = map_phys(row_pt, raw);
+      }
     }
-    return;
+    return;  // the merge's short rows are finish_rows_team_kernel's
+  }
+  if constexpr (!DENSE) {
+    if (p.blocks[p.row_block[r]].n_units == 1) return;  // finish_rows_team_kernel's
   }
 
   if (tid == 0) {
@@ -111,27 +347,20 @@ __global__ void __launch_bounds__(kFinThreads) finish_kernel(FinishParams p) {
     for (int i = n + tid; i < TOPK; i += kFinThreads) buf[i] = 0ull;
   }
   __syncthreads();
-  // bitonic sort, descending by key (score desc, then index asc)
-  for (int size = 2; size <= TOPK; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < TOPK / 2; i += kFinThreads) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const uint64_t a = buf[lo], c = buf[hi];
-        const bool desc = (lo & size) == 0;
-        if (desc ? (a < c) : (a > c)) {
-          buf[lo] = c;
-          buf[hi] = a;
-        }
-      }
-      __syncthreads();
-    }
-  }
-  for (int i = tid; i < TOPK; i += kFinThreads) {
-    const uint64_t key = buf[i];
-    const int32_t raw = key != 0ull ? key_index(key) : -1;
-    if (out_raw) out_raw[i] = raw;
-    if (out_phys) out_phys[i] = map_phys(row_pt, raw);
+  sort_emit<TOPK>(buf, tid, row_pt, out_raw, out_phys);
+}
+
+// Rows strided over the grid; the status is read once per row by one thread
+// so that the CTA's threads agree on it.
+template <int TOPK, bool DENSE>
+__global__ void __launch_bounds__(kFinThreads) finish_kernel(FinishParams p) {
+  __shared__ __align__(16) FinSmem sm;
+  for (int64_t r = blockIdx.x; r < p.rows; r += gridDim.x) {
+    if (threadIdx.x == 0) sm.ok = read_status(p.hdr) == kOk;
+    __syncthreads();
+    if (!sm.ok) return;
+    finish_row<TOPK, DENSE>(p, r, sm);
+    __syncthreads();  // the row's shared state is free again
   }
 }
 
@@ -147,7 +376,13 @@ __global__ void validate_windows_kernel(const int32_t* row_start, const int32_t*
 
 template <int TOPK, bool DENSE>
 cudaError_t launch_t(const FinishParams& p, cudaStream_t stream) {
-  finish_kernel<TOPK, DENSE><<<p.rows, kFinThreads, 0, stream>>>(p);
+  if (!DENSE) {
+    constexpr int kTeams = kTeamThreads / 32 / (TOPK / kTeamKeys);
+    const int grid = (p.rows + kTeams - 1) / kTeams;
+    finish_rows_team_kernel<TOPK><<<grid, kTeamThreads, 0, stream>>>(p);
+  }
+  const int grid = p.rows < kFinGridCap ? p.rows : kFinGridCap;
+  finish_kernel<TOPK, DENSE><<<grid, kFinThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -190,7 +425,10 @@ __global__ void __launch_bounds__(kFinThreads) tile_merge_kernel(TileMergeParams
   __shared__ uint64_t tau;
   const int r = blockIdx.x;
   const int tid = threadIdx.x;
-  if (read_status(p.hdr) != kOk) return;
+  __shared__ uint32_t ok;  // one status read, so that the CTA's threads agree
+  if (tid == 0) ok = read_status(p.hdr) == kOk;
+  __syncthreads();
+  if (!ok) return;
   const int32_t s0 = p.row_start[r], s1 = p.row_end[r];
   const int64_t len = (int64_t)s1 - s0;
   const int32_t* row_pt = p.page_table + (int64_t)p.row_req[r] * p.max_pages;
@@ -245,27 +483,8 @@ __global__ void __launch_bounds__(kFinThreads) tile_merge_kernel(TileMergeParams
     for (int i = n + tid; i < TOPK; i += kFinThreads) buf[i] = 0ull;
   }
   __syncthreads();
-  for (int size = 2; size <= TOPK; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < TOPK / 2; i += kFinThreads) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const uint64_t x = buf[lo], y = buf[hi];
-        const bool desc = (lo & size) == 0;
-        if (desc ? (x < y) : (x > y)) {
-          buf[lo] = y;
-          buf[hi] = x;
-        }
-      }
-      __syncthreads();
-    }
-  }
-  for (int i = tid; i < TOPK; i += kFinThreads) {
-    const uint64_t key = buf[i];
-    const int32_t raw = key != 0ull ? key_index(key) : -1;
-    if (p.out_raw) p.out_raw[(int64_t)r * TOPK + i] = raw;
-    p.out_phys[(int64_t)r * TOPK + i] = map_phys(row_pt, raw);
-  }
+  sort_emit<TOPK>(buf, tid, row_pt, p.out_raw ? p.out_raw + (int64_t)r * TOPK : nullptr,
+                  p.out_phys + (int64_t)r * TOPK);
 }
 }  // namespace
 

@@ -323,7 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   PlanHeader* hdr = p.hdr;
-  if (read_status(hdr) != kOk) return;
+  // after an earlier error no unit is run; all threads take the same decision
+  if (__syncthreads_or(read_status(hdr) != kOk)) return;
   const int n_units = hdr->n_units;
 
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * (uint32_t)i; };
