@@ -40,6 +40,7 @@ L2_FLUSH_BYTES = 256 << 20
 EPI_OPS_PER_ELEMENT = 2               # ReLU max + weighted multiply-add per (row, head, slot)
 FP32_LANES_PER_SM = 128               # 4 partitions x 32 FP32 lanes
 NOMINAL_SM_MHZ = 2070.0
+KERNELS_PER_CALL = 5                  # plan, page check, scorer, row-team sort, multi-unit merge
 
 
 def parse_args():
@@ -327,7 +328,7 @@ def main():
                        "algorithmic_flop": flop,
                        "l2": "flushed before every timed step (256 MiB write, untimed)",
                        "parallelism": f"replicas x{world} (rows independent; no collective)"},
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": KERNELS_PER_CALL * args.steps,
             "clocks": clk,
             "e2e": {"value": whole_job_tflops(flop, world, e2e_step), "unit": "TFLOP/s",
                     "ms_per_step": e2e_step, "h2d_bytes_per_step": h2d,
