@@ -115,3 +115,29 @@ def test_full_size_workload(cfg):
     torch.cuda.empty_cache()
     dp, dr = H.run_dense(p, d)
     assert np.array_equal(dp, g_phys) and np.array_equal(dr, g_raw)
+
+
+@pytest.mark.parametrize("topk", [512, 1024])
+def test_768k_context(topk):
+    # the context length of the memory-geometry example of "[AMD][DSv4] Add
+    # experimental AITER FP4 streaming TopK" (sglang#38101): one request of
+    # 786,432 C4 positions (12,288 pages); causal rows at its end, windows that
+    # start far from 0, the len == K and len == K + 1 boundaries, an empty row
+    import torch
+    L = 786432
+    wins = [(0, L - 3 + j) for j in range(4)] + [
+        (100000, 700001), (0, L), (L - topk - 1, L), (5, 5 + topk), (400000, 400000),
+        (L // 2 + 7, L // 2 + 7 + 3 * topk)]
+    p = inputs.make_problem(31, [L], [wins], topk=topk, name=f"ctx768k-K{topk}")
+    d = H.to_device(p)
+    code, g_phys, g_raw = H.run_fused(p, d)
+    assert code == 0
+    rows = np.arange(p.rows, dtype=np.int32)
+    o_phys, o_raw, _, inexact = oracle.prefill_rows(p, rows=rows, with_kth=True)
+    assert inexact == 0
+    scores = {int(r): oracle.row_scores(p, int(r))[0] for r in rows if p.lengths()[r] > p.topk}
+    assert H.compare_rows(p, rows, g_raw, g_phys, o_raw, o_phys, scores) <= 2
+    sc, _ = H.run_debug(p, d)
+    check_exact_topk_on_device(p, sc, g_raw, g_phys)
+    del sc
+    torch.cuda.empty_cache()
