@@ -31,6 +31,11 @@ __device__ __forceinline__ int32_t map_phys(const int32_t* row_pt, int32_t raw) 
   return (int32_t)v;
 }
 
+// keep the larger (or smaller) of each register and its partner's
+__device__ __forceinline__ uint64_t keep_of(uint64_t x, uint64_t o, bool keep_max) {
+  return (x > o) == keep_max ? x : o;  // equal keys: either
+}
+
 // One bitonic step at distance S (< E) between a thread's own keys t*E + e.
 template <int E, int S>
 __device__ __forceinline__ void sort_in_thread(uint64_t (&v)[E], int g0, int size) {
@@ -39,7 +44,7 @@ __device__ __forceinline__ void sort_in_thread(uint64_t (&v)[E], int g0, int siz
     if ((e & S) != 0) continue;
     const bool desc = ((g0 + e) & size) == 0;
     const uint64_t a = v[e], b = v[e | S];
-    const bool sw = desc ? (a < b) : (a > b);
+    const bool sw = (a < b) == desc;  // equal keys (zero padding) may swap
     v[e] = sw ? b : a;
     v[e | S] = sw ? a : b;
   }
@@ -79,7 +84,7 @@ __device__ __forceinline__ void sort_emit(uint64_t* buf, int tid, const int32_t*
 #pragma unroll
           for (int e = 0; e < E; ++e) {
             const uint64_t o = __shfl_xor_sync(0xffffffffu, v[e], stride / E);
-            v[e] = keep_max ? (v[e] > o ? v[e] : o) : (v[e] < o ? v[e] : o);
+            v[e] = keep_of(v[e], o, keep_max);
           }
         } else {
           __syncthreads();  // earlier readers of buf are done
@@ -89,7 +94,7 @@ __device__ __forceinline__ void sort_emit(uint64_t* buf, int tid, const int32_t*
 #pragma unroll
           for (int e = 0; e < E; ++e) {
             const uint64_t o = buf[(g0 + e) ^ stride];
-            v[e] = keep_max ? (v[e] > o ? v[e] : o) : (v[e] < o ? v[e] : o);
+            v[e] = keep_of(v[e], o, keep_max);
           }
         }
       }
@@ -134,15 +139,10 @@ __device__ __forceinline__ void team_reg_step(uint64_t (&v)[kTeamE], int g0, int
     if ((e & S) != 0) continue;
     const bool desc = ((g0 + e) & size) == 0;
     const uint64_t a = v[e], b = v[e | S];
-    const bool sw = desc ? (a < b) : (a > b);
+    const bool sw = (a < b) == desc;  // equal keys (zero padding) may swap
     v[e] = sw ? b : a;
     v[e | S] = sw ? a : b;
   }
-}
-
-// keep the larger (or smaller) of each register and its partner's
-__device__ __forceinline__ uint64_t keep_of(uint64_t x, uint64_t o, bool keep_max) {
-  return keep_max ? (x > o ? x : o) : (x < o ? x : o);
 }
 
 // The network over N keys.  The loops over block sizes and distances stay
