@@ -256,6 +256,8 @@ __global__ void __launch_bounds__(kTeamThreads) finish_rows_team_kernel(FinishPa
 struct FinSmem {
   uint64_t buf[kFinCap];
   uint32_t hist[256];
+  uint32_t uoff[kFinThreads];           // first buffer position of each unit's keys
+  uint32_t wsum[kFinThreads / 32];
   uint32_t bc[4];
   uint32_t cnt;
   uint32_t ok;
@@ -317,8 +319,50 @@ __device__ __forceinline__ void finish_row(const FinishParams& p, int64_t r, Fin
     }
   } else {
     const BlockInfo bi = p.blocks[p.row_block[r]];
-    const int j = r - bi.row0;
-    for (int k = 0; k < bi.n_units; ++k) {
+    const int j = (int)(r - bi.row0);
+    // When the row's units hold at most kFinCap keys together, gather them all
+    // at once (unit u's keys to buf[uoff[u] ..]) instead of unit by unit.
+    bool gathered = false;
+    if (bi.n_units <= kFinThreads) {
+      uint32_t c = 0;
+      if (tid < bi.n_units)
+        c = min(p.cand_cnt[bi.slot0 + (int64_t)tid * bi.nrows + j], (uint32_t)TOPK);
+      const int lane = tid & 31, w = tid >> 5;
+      uint32_t x = c;  // inclusive scan of the counts: lanes, then warps
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) sm.wsum[w] = x;
+      __syncthreads();
+      uint32_t before = 0, total = 0;
+#pragma unroll
+      for (int k = 0; k < kFinThreads / 32; ++k) {
+        const uint32_t ws = sm.wsum[k];
+        before += k < w ? ws : 0u;
+        total += ws;
+      }
+      sm.uoff[tid] = before + x - c;
+      __syncthreads();
+      if (total <= (uint32_t)kFinCap) {  // the same decision in every thread
+        for (uint32_t i = tid; i < total; i += kFinThreads) {
+          // the last unit starting at or before i (units without keys share
+          // their successor's start and are skipped this way)
+          int lo = 0, hi = bi.n_units - 1;
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (sm.uoff[mid] <= i) lo = mid;
+            else hi = mid - 1;
+          }
+          const int64_t slot = bi.slot0 + (int64_t)lo * bi.nrows + j;
+          buf[i] = p.cand_keys[slot * TOPK + (i - sm.uoff[lo])];
+        }
+        if (tid == 0) cnt = total;
+        gathered = true;
+      }
+    }
+    for (int k = 0; !gathered && k < bi.n_units; ++k) {
       const int64_t slot = bi.slot0 + (int64_t)k * bi.nrows + j;
       const uint32_t n = min(p.cand_cnt[slot], (uint32_t)TOPK);
       const uint64_t* keys = p.cand_keys + slot * TOPK;

@@ -303,6 +303,8 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   int blocks = p.grid > 0 ? p.grid * 4 : 128;
+  const int need = (p.rows + 7) / 8;  // one warp per row block, at most one block per row
+  if (blocks > need) blocks = need > 0 ? need : 1;
   validate_pages_kernel<<<blocks, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
