@@ -20,6 +20,7 @@ import ctypes
 from . import _lib
 
 __all__ = ["IdxError", "SUPPORTED_K", "idx_topk_fp4_prefill", "idx_topk_fp4_prefill_noalloc",
+           "idx_topk_fp4_prefill_host",
            "idx_topk_fp4_prefill_async", "idx_topk_fp4_prefill_paged",
            "idx_dense_topk_fp4_prefill", "idx_tiled_topk_fp4_prefill",
            "idx_fp4_debug_scores", "idx_topk_select_scores", "idx_topk_supported_k",
@@ -82,6 +83,23 @@ def idx_topk_fp4_prefill(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_tab
     code = lib.idx_topk_fp4_prefill(*[_ref(d) for d in ds[:9]], int(topk), _ref(ds[9]),
                                     _ref(ds[10]), _stream(stream))
     return _check(code, "idx_topk_fp4_prefill", raise_on_error)
+
+
+def idx_topk_fp4_prefill_host(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                              row_start, row_end, topk, out_phys_slot, out_raw_idx=None, device=0,
+                              stream=None, raise_on_error=True) -> int:
+    """idx_topk_fp4_prefill on CPU tensors (pinned for asynchronous copies): the
+    library stages them on `device`, runs the fused path and writes the CPU
+    outputs in place before returning."""
+    import torch
+    lib = _lib.load()
+    ds = [_desc(t) for t in (q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                             row_start, row_end, out_phys_slot, out_raw_idx)]
+    if stream is None:
+        stream = torch.cuda.current_stream(int(device))
+    code = lib.idx_topk_fp4_prefill_host(*[_ref(d) for d in ds[:9]], int(topk), _ref(ds[9]),
+                                         _ref(ds[10]), int(device), _stream(stream))
+    return _check(code, "idx_topk_fp4_prefill_host", raise_on_error)
 
 
 def idx_topk_fp4_prefill_paged(q_fp4, q_scale, k_pages, weights, page_table, row_req, row_start,

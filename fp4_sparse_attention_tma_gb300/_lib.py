@@ -87,6 +87,9 @@ EXPORTS = {
                                    [ctypes.c_int32, ctypes.POINTER(IdxTensor),
                                     ctypes.POINTER(IdxTensor), ctypes.c_void_p, ctypes.c_uint64,
                                     ctypes.c_void_p, ctypes.c_void_p]),
+    "idx_topk_fp4_prefill_host": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
+                                  [ctypes.c_int32, ctypes.POINTER(IdxTensor),
+                                   ctypes.POINTER(IdxTensor), ctypes.c_int32, ctypes.c_void_p]),
     "idx_topk_fp4_prefill_noalloc": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
                                      [ctypes.c_int32, ctypes.POINTER(IdxTensor),
                                       ctypes.POINTER(IdxTensor), ctypes.c_void_p]),

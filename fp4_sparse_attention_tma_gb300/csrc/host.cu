@@ -123,8 +123,9 @@ bool mul_ok(int64_t a, int64_t b, int64_t* out) {
 }
 
 // Validates one descriptor: dtype, rank, non-negative shape, C-contiguous
-// strides, 16-byte aligned base (unless empty).  Returns IDX_OK or an error.
-int check_tensor(const idx_tensor_t* t, int dtype, int ndim) {
+// strides, 16-byte aligned base (unless empty or need_align is false: host
+// tensors that are only copied).  Returns IDX_OK or an error.
+int check_tensor(const idx_tensor_t* t, int dtype, int ndim, bool need_align = true) {
   if (!t) return IDX_ERR_INVALID_ARGUMENT;
   if (t->dtype != dtype || t->ndim != ndim) return IDX_ERR_INVALID_ARGUMENT;
   int64_t numel = 1;
@@ -141,7 +142,7 @@ int check_tensor(const idx_tensor_t* t, int dtype, int ndim) {
   if (!mul_ok(numel, dtype == IDX_U8 ? 1 : 4, &bytes)) return IDX_ERR_OVERFLOW;
   if (numel > 0) {
     if (!t->data) return IDX_ERR_INVALID_ARGUMENT;
-    if (((uintptr_t)t->data & 15u) != 0) return IDX_ERR_INVALID_ARGUMENT;
+    if (need_align && ((uintptr_t)t->data & 15u) != 0) return IDX_ERR_INVALID_ARGUMENT;
   }
   return IDX_OK;
 }
@@ -252,8 +253,8 @@ int check_inputs(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
   return IDX_OK;
 }
 
-int check_output(const idx_tensor_t* out, int64_t rows, int32_t topk) {
-  int st = check_tensor(out, IDX_I32, 2);
+int check_output(const idx_tensor_t* out, int64_t rows, int32_t topk, bool need_align = true) {
+  int st = check_tensor(out, IDX_I32, 2, need_align);
   if (st) return st;
   if (out->shape[0] != rows || out->shape[1] != topk) return IDX_ERR_INVALID_ARGUMENT;
   return IDX_OK;
@@ -1044,6 +1045,105 @@ int run_stream_ordered(const Call& c, void* workspace, uint64_t workspace_bytes,
   return IDX_OK;
 }
 
+// ---------------------------------------------------- host-buffer call ----
+//
+// idx_topk_fp4_prefill_host: the inputs and outputs live in host memory.  The
+// call stages them through one block of the device's pool (one
+// cudaMemcpyAsync per tensor on the caller's stream), runs the fused path on
+// the staged copies and copies the outputs back.
+
+// True when t is empty or its data is host memory (pageable or pinned).
+bool is_host_tensor(const idx_tensor_t* t) {
+  if (!t || numel_of(t) == 0) return true;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, t->data) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost || a.type == cudaMemoryTypeUnregistered;
+}
+
+size_t tensor_bytes(const idx_tensor_t* t) {
+  return t ? (size_t)numel_of(t) * (t->dtype == IDX_U8 ? 1u : 4u) : 0u;
+}
+
+int run_host(const Call& h, int32_t device, cudaStream_t stream) {
+  const int64_t R = h.q_fp4 ? h.q_fp4->shape[0] : 0;
+  int st = check_output(h.out_phys, R, h.topk, false);
+  if (st) return st;
+  if (h.out_raw && (st = check_output(h.out_raw, R, h.topk, false))) return st;
+  if (!is_host_tensor(h.out_phys) || !is_host_tensor(h.out_raw)) return IDX_ERR_INVALID_ARGUMENT;
+  const idx_tensor_t* outs[2] = {h.out_phys, h.out_raw};
+  auto host_fail = [&](int code) {
+    for (const idx_tensor_t* t : outs)
+      if (t && numel_of(t) > 0) std::memset(t->data, 0xFF, tensor_bytes(t));
+    return code;
+  };
+  const idx_tensor_t* in[9] = {h.q_fp4, h.q_scale, h.k_cache_fp4, h.k_scale, h.weights,
+                               h.page_table, h.row_req, h.row_start, h.row_end};
+  const int in_dtype[9] = {IDX_U8, IDX_U8, IDX_U8, IDX_U8, IDX_F32, IDX_I32, IDX_I32, IDX_I32, IDX_I32};
+  const int in_ndim[9] = {3, 3, 3, 3, 2, 2, 1, 1, 1};
+  for (int i = 0; i < 9; ++i) {
+    if ((st = check_tensor(in[i], in_dtype[i], in_ndim[i], false))) return host_fail(st);
+    if (!is_host_tensor(in[i])) return host_fail(IDX_ERR_INVALID_ARGUMENT);
+  }
+  int n_dev = 0;
+  if (cudaGetDeviceCount(&n_dev) != cudaSuccess) {
+    cudaGetLastError();
+    return host_fail(IDX_ERR_CUDA);
+  }
+  if (device < 0 || device >= n_dev) return host_fail(IDX_ERR_INVALID_ARGUMENT);
+  DeviceGuard guard(device);
+  if (!guard.ok()) return host_fail(IDX_ERR_CUDA);
+  if ((st = check_stream(stream, device))) return host_fail(st);
+  if (R == 0) return IDX_OK;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(device, &ds))) return host_fail(st);
+  // staging layout: the nine inputs, then the two outputs, 256-byte aligned
+  size_t off[11], total = 0;
+  const idx_tensor_t* all[11] = {in[0], in[1], in[2], in[3], in[4], in[5], in[6], in[7], in[8],
+                                 h.out_phys, h.out_raw};
+  for (int i = 0; i < 11; ++i) {
+    off[i] = total;
+    total = align_up(total + tensor_bytes(all[i]), 256);
+  }
+  void* base = nullptr;
+  if (cudaMallocFromPoolAsync(&base, total, ds->pool, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return host_fail(IDX_ERR_CUDA);
+  }
+  idx_tensor_t dev_t[11];
+  bool cuda_ok = true;
+  for (int i = 0; i < 11; ++i) {
+    if (!all[i]) continue;
+    dev_t[i] = *all[i];
+    const size_t bytes = tensor_bytes(all[i]);
+    dev_t[i].data = bytes ? (char*)base + off[i] : nullptr;
+    if (i < 9 && bytes)
+      cuda_ok &= cudaMemcpyAsync(dev_t[i].data, all[i]->data, bytes, cudaMemcpyHostToDevice,
+                                 stream) == cudaSuccess;
+  }
+  int code = IDX_ERR_CUDA;
+  if (cuda_ok) {
+    Call c{&dev_t[0], &dev_t[1], &dev_t[2], &dev_t[3], &dev_t[4], &dev_t[5], &dev_t[6], &dev_t[7],
+           &dev_t[8], h.topk, &dev_t[9], h.out_raw ? &dev_t[10] : nullptr, nullptr, nullptr,
+           Path::kFused};
+    code = run(c, stream);
+  }
+  if (code == IDX_OK)
+    for (int i = 9; i < 11; ++i)
+      if (all[i] && tensor_bytes(all[i]))
+        cuda_ok &= cudaMemcpyAsync(all[i]->data, dev_t[i].data, tensor_bytes(all[i]),
+                                   cudaMemcpyDeviceToHost, stream) == cudaSuccess;
+  cuda_ok &= cudaFreeAsync(base, stream) == cudaSuccess;
+  cuda_ok &= cudaStreamSynchronize(stream) == cudaSuccess;
+  if (!cuda_ok) {
+    cudaGetLastError();
+    return host_fail(IDX_ERR_CUDA);
+  }
+  return code == IDX_OK ? IDX_OK : host_fail(code);
+}
+
 const int32_t kSupportedK[2] = {512, 1024};
 
 }  // namespace
@@ -1060,6 +1160,18 @@ int idx_topk_fp4_prefill(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
   Call c{q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req, row_start, row_end,
          topk, out_phys_slot, out_raw_idx, nullptr, nullptr, Path::kFused};
   return run(c, (cudaStream_t)stream);
+}
+
+int idx_topk_fp4_prefill_host(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                              const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
+                              const idx_tensor_t* weights, const idx_tensor_t* page_table,
+                              const idx_tensor_t* row_req, const idx_tensor_t* row_start,
+                              const idx_tensor_t* row_end, int32_t topk,
+                              const idx_tensor_t* out_phys_slot, const idx_tensor_t* out_raw_idx,
+                              int32_t device, idx_stream_t stream) {
+  Call c{q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req, row_start, row_end,
+         topk, out_phys_slot, out_raw_idx, nullptr, nullptr, Path::kFused};
+  return run_host(c, device, (cudaStream_t)stream);
 }
 
 int idx_topk_fp4_prefill_noalloc(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,

@@ -135,6 +135,33 @@ int idx_topk_fp4_prefill_paged(const idx_tensor_t* q_fp4, const idx_tensor_t* q_
                                const idx_tensor_t* out_raw_idx, idx_stream_t stream);
 
 /*
+ * idx_topk_fp4_prefill on tensors in host memory (the pages have no
+ * counterpart: it serves callers whose query block, K cache and metadata sit
+ * in host memory, and it is the end-to-end form of the operation, host copies
+ * included).
+ *   device  the GPU to run on (0 .. count-1); stream must belong to it or be NULL.
+ * Every descriptor points to host memory: pinned memory (cudaHostAlloc or
+ * cudaHostRegister) makes the copies asynchronous DMA; pageable memory also
+ * works, at host-copy speed.  Shapes, dtypes and results are those of
+ * idx_topk_fp4_prefill; host buffers need no particular alignment.  The call
+ * takes one block of device memory from the library's stream-ordered pool,
+ * copies each input into it (one cudaMemcpyAsync per tensor on `stream`), runs
+ * the fused path there, copies the outputs back, returns the block to the pool
+ * and returns once `stream` has completed.  It keeps no pointer.  Error codes
+ * are those of idx_topk_fp4_prefill; a descriptor that points to device memory
+ * or a device index out of range is IDX_ERR_INVALID_ARGUMENT.  On any error
+ * after the output descriptors are validated, the host outputs are filled
+ * with -1.
+ */
+int idx_topk_fp4_prefill_host(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                              const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
+                              const idx_tensor_t* weights, const idx_tensor_t* page_table,
+                              const idx_tensor_t* row_req, const idx_tensor_t* row_start,
+                              const idx_tensor_t* row_end, int32_t topk,
+                              const idx_tensor_t* out_phys_slot, const idx_tensor_t* out_raw_idx,
+                              int32_t device, idx_stream_t stream);
+
+/*
  * Stream-ordered variant of idx_topk_fp4_prefill for decode loops and CUDA
  * graphs: the same operation and outputs, with no allocation and no host
  * synchronisation, so a call may be captured into a graph and replayed.  The
