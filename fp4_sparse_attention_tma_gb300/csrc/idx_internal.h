@@ -26,8 +26,13 @@ constexpr int kRowsPerBlock = 3;    // query rows sharing one K tile (one per ep
 constexpr int kRowsPerChunk = 1;    // query rows per TMA box of the query block (64 head rows)
 constexpr int kChunks = kRowsPerBlock / kRowsPerChunk;
 constexpr int kAccStages = 2;       // TMEM accumulator buffers (double buffer, N = 3 x 64 each)
-constexpr int kMinUnitTiles = 32;   // shortest work unit (tiles), except whole short blocks
-constexpr int kUnitsPerCta = 4;     // target work units per persistent CTA
+// Work-unit sizing: the planner cuts a block's tiles into units of about
+// max(total tiles / SMs, kMinUnitTiles) tiles.  About one unit per persistent
+// CTA keeps the per-unit costs (query-block load, threshold warm-up, final
+// selection and candidate write) and the merge of a row's units small; the
+// longest-first, alternating deal of the units keeps the CTAs balanced.
+constexpr int kMinUnitTiles = 64;   // shortest work unit (tiles), except whole short blocks
+constexpr int kUnitsPerCta = 1;     // target work units per persistent CTA
 
 // Status codes (mirror idx_status_t of the public header).
 enum : uint32_t {

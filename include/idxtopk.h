@@ -24,7 +24,8 @@
  *
  * Conventions for every entry point:
  *  - Tensors are passed as idx_tensor_t descriptors of DEVICE memory that the
- *    caller owns; the library keeps no pointer after it returns.  All tensors
+ *    caller owns (idx_topk_fp4_prefill_host alone takes host memory); the
+ *    library keeps no pointer after it returns.  All tensors
  *    of a call must live on one device; the call makes that device current for
  *    its duration and restores the caller's current device before returning
  *    (aiter#5309 Implementation: caller device/stream ownership).
@@ -211,9 +212,9 @@ int idx_topk_fp4_prefill_async(const idx_tensor_t* q_fp4, const idx_tensor_t* q_
  * buffer of IDX_NOALLOC_SCRATCH_BYTES per device that is part of the
  * library's device image, so the call makes no cudaMalloc/cudaFree, pool or
  * event allocation.  Its size need is idx_topk_fp4_scratch_bytes(rows, topk):
- * (rows + 12 * SMs) * topk * 8 bytes plus a few KB; a call that needs more
+ * (rows + 3 * SMs) * topk * 8 bytes plus a few KB; a call that needs more
  * returns IDX_ERR_SCRATCH_LIMIT (outputs filled with -1) without running.
- * At 152 SMs that admits up to about 4,280 rows at topk 1024 and 10,290 at 512.
+ * At 152 SMs that admits up to about 5,640 rows at topk 1024 and 11,630 at 512.
  *
  *  - The first call on a device looks up the buffer's address there (the
  *    device is made current for it); make that first call before any stream
