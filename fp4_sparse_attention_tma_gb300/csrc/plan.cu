@@ -209,8 +209,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   if (read_status(hdr) != kOk) return;
 
   // 5. schedule: longest units first (the scorer deals them to its persistent
-  //    CTAs band by band, alternating the direction)
-  if (n_units <= kSortMax) {
+  //    CTAs band by band, alternating the direction).  With no more units than
+  //    CTAs every unit starts at once and the order cannot matter.
+  if (n_units > p.grid && n_units <= kSortMax) {
     int64_t n2 = 1;
     while (n2 < n_units) n2 <<= 1;
     for (int64_t i = tid; i < n2; i += kPlanThreads) {
@@ -279,14 +280,23 @@ __global__ void __launch_bounds__(256) validate_pages_kernel(PlanParams p) {
     const int32_t p0 = lo / kPage, p1 = (hi + kPage - 1) / kPage;
     const int32_t* row_pt = p.page_table + (int64_t)bi.req * p.max_pages;
     bool bad = false;
-    for (int32_t pg = p0 + lane; pg < p1; pg += 32) {
-      bool need = false;
-      for (int j = 0; j < kRowsPerBlock; ++j)
-        need |= (s[j] < (pg + 1) * kPage) && (e[j] > pg * kPage) && (e[j] > s[j]);
-      if (need) {
-        int32_t v = row_pt[pg];
-        bad |= (v < 0) || (v >= p.num_pages);
+    // kPtUnroll independent entry loads per lane are in flight before any is
+    // checked (a long window has thousands of entries)
+    constexpr int kPtUnroll = 8;
+    for (int32_t base = p0; base < p1; base += 32 * kPtUnroll) {
+      int32_t v[kPtUnroll];
+      bool need[kPtUnroll];
+#pragma unroll
+      for (int u = 0; u < kPtUnroll; ++u) {
+        const int32_t pg = base + 32 * u + lane;
+        need[u] = false;
+        if (pg < p1)
+          for (int j = 0; j < kRowsPerBlock; ++j)
+            need[u] |= (s[j] < (pg + 1) * kPage) && (e[j] > pg * kPage) && (e[j] > s[j]);
+        v[u] = need[u] ? row_pt[pg] : 0;
       }
+#pragma unroll
+      for (int u = 0; u < kPtUnroll; ++u) bad |= need[u] && ((v[u] < 0) || (v[u] >= p.num_pages));
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) raise_status(hdr, kErrInvalidPage, 120);
   }
