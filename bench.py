@@ -38,7 +38,8 @@ FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 EPI_OPS_PER_ELEMENT = 2               # ReLU max + weighted multiply-add per (row, head, slot)
-FP32_LANES_PER_SM = 128               # 4 partitions x 32 FP32 lanes
+FP32_LANES_PER_SM = 128               # 4 partitions x 32 lanes, one warp instruction per clock each
+EPI_OPS_PER_ISSUE = 4.0 / 3.0         # per head pair: two max.f32 + one fma.rn.f32x2 = 4 ops, 3 issues
 NOMINAL_SM_MHZ = 2070.0
 KERNELS_PER_CALL = 5                  # plan, page check, scorer, row-team sort, multi-unit merge
 
@@ -346,16 +347,20 @@ def main():
                         "peak_source": f"{src} bf16 burst x {NOMINAL_FP4_OVER_BF16:g} "
                                        "(nominal dense FP4/bf16 ratio)"}
     # the epilogue's CUDA-core roof: per (row, head, slot) element one ReLU
-    # (max with 0) and one weighted accumulate, on 128 FP32 lanes per SM
+    # (max with 0) and one weighted accumulate; a head pair takes two max.f32
+    # and one packed fma.rn.f32x2, 4 operations in 3 issue slots, at one warp
+    # instruction per clock per SM partition (128 lanes per SM)
     sms = torch.cuda.get_device_properties(local).multi_processor_count
     elem_ops = float(p.scored_pairs()) * 64 * EPI_OPS_PER_ELEMENT
-    alu_peak = sms * FP32_LANES_PER_SM * float(clk.get("sm_max_mhz") or NOMINAL_SM_MHZ) * 1e6 / 1e12
+    alu_peak = (sms * FP32_LANES_PER_SM * EPI_OPS_PER_ISSUE *
+                float(clk.get("sm_max_mhz") or NOMINAL_SM_MHZ) * 1e6 / 1e12)
     alu_achieved = elem_ops / (sc * 1e-3) / 1e12
     line["roofline_alu"] = {"bound": "alu", "achieved": alu_achieved, "peak": alu_peak,
                             "unit": "Tops/s", "frac": alu_achieved / alu_peak,
                             "ops_per_launch": elem_ops,
-                            "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x "
-                                           "max SM clock"}
+                            "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} lanes x 4/3 "
+                                           "ops per issue (2 max + 1 packed FMA per head "
+                                           "pair) x max SM clock"}
     line["phases_ms"] = {"kernels": statistics.mean(kern_ms), "score": sc}
     line["scratch"] = {"bytes_per_call": m.idx_topk_fp4_scratch_bytes(R, K, local),
                        "pool_high_water": m.idx_topk_scratch_high_water(local),
