@@ -61,6 +61,22 @@ def test_page_entries_outside_windows_are_not_read(base):
     assert code == 0
 
 
+@pytest.mark.parametrize("page,expect", [(900, 4), (937, 4), (938, 0), (1020, 0)])
+def test_page_check_covers_long_windows(page, expect):
+    # one row whose window [0, 60000) spans logical pages 0..937 of a
+    # 1024-page request: an invalid entry anywhere under it fails the call
+    # closed; entries past the window's last page are never read
+    p = inputs.make_problem(52, [65536, 64], [[(0, 60000)], [(0, 64)]], topk=512)
+    d = H.to_device(p)
+    d["page_table"][0, page] = -5 if expect else 987654321
+    code, phys, raw = _call(p, d)
+    assert code == expect
+    if expect:
+        assert np.all(phys == -1) and np.all(raw == -1)
+    else:
+        assert (raw[0] >= 0).all()
+
+
 @pytest.mark.parametrize("field,value,row", [("row_req", 5, 1), ("row_req", -1, 0),
                                              ("row_start", -3, 2), ("row_end", 10**6, 0),
                                              ("row_start", 1600, 2)])
