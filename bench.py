@@ -41,7 +41,7 @@ EPI_OPS_PER_ELEMENT = 2               # ReLU max + weighted multiply-add per (ro
 FP32_LANES_PER_SM = 128               # 4 partitions x 32 lanes, one warp instruction per clock each
 EPI_OPS_PER_ISSUE = 4.0 / 3.0         # per head pair: two max.f32 + one fma.rn.f32x2 = 4 ops, 3 issues
 NOMINAL_SM_MHZ = 2070.0
-KERNELS_PER_CALL = 5                  # plan, page check, scorer, row-team sort, multi-unit merge
+KERNELS_PER_CALL = 4                  # plan, page check, scorer, finish (row-team sort + multi-unit merge in one launch)
 
 
 def parse_args():

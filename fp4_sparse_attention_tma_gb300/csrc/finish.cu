@@ -23,7 +23,7 @@ constexpr int kFinCap = 4096;
 constexpr int kFinPer = 4;  // keys per thread per batch
 constexpr int kFinBatch = kFinThreads * kFinPer;
 constexpr uint32_t kFinBar = 1;
-constexpr int kFinGridCap = 2048;  // CTAs of finish_kernel (rows strided over them)
+constexpr int kFinGridCap = 2048;  // merging CTAs (rows strided over them)
 
 __device__ __forceinline__ int32_t map_phys(const int32_t* row_pt, int32_t raw) {
   if (raw < 0 || row_pt == nullptr) return -1;
@@ -126,7 +126,7 @@ __device__ __forceinline__ void sort_emit(uint64_t* buf, int tid, const int32_t*
 // between the lanes of a warp, 512 (TOPK = 1024 only) through shared memory
 // between the team's two warps.  The teams also handle every short row
 // (length <= TOPK: start .. end-1, then -1).  Rows of multi-unit blocks are
-// left to finish_kernel.
+// left to merge_rows.
 constexpr int kTeamThreads = 256;
 constexpr int kTeamE = 16;          // keys per lane
 constexpr int kTeamKeys = 32 * kTeamE;
@@ -188,16 +188,25 @@ __device__ __forceinline__ void team_sort(uint64_t (&v)[kTeamE], int g0, int lan
 }
 
 template <int TOPK>
-__global__ void __launch_bounds__(kTeamThreads) finish_rows_team_kernel(FinishParams p) {
-  constexpr int W = TOPK / kTeamKeys;  // warps per row
-  constexpr int kTeams = kTeamThreads / 32 / W;
-  __shared__ __align__(16) uint64_t xbuf[W == 2 ? kTeams * TOPK : 1];
-  __shared__ uint32_t team_ok[kTeams];
+struct TeamSmem {
+  static constexpr int W = TOPK / kTeamKeys;             // warps per row
+  static constexpr int kTeams = kTeamThreads / 32 / W;   // rows per CTA
+  uint64_t xbuf[W == 2 ? kTeams * TOPK : 1];
+  uint32_t team_ok[kTeams];
+};
+
+// The rows of CTA `blk` of the team grid (kTeams rows per CTA).
+template <int TOPK>
+__device__ __forceinline__ void team_rows(const FinishParams& p, int64_t blk, TeamSmem<TOPK>& ts) {
+  constexpr int W = TeamSmem<TOPK>::W;
+  constexpr int kTeams = TeamSmem<TOPK>::kTeams;
+  uint64_t* xbuf = ts.xbuf;
+  uint32_t* team_ok = ts.team_ok;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int team = warp / W, tw = warp % W;
   const uint32_t bar_id = 1u + (uint32_t)team;
-  const int64_t r = (int64_t)blockIdx.x * kTeams + team;
+  const int64_t r = blk * kTeams + team;
   if (r >= p.rows) return;  // the same for both warps of a team
   // one status read per team, so that its warps take the same path
   if (tw == 0 && lane == 0) team_ok[team] = read_status(p.hdr) == kOk;
@@ -288,10 +297,10 @@ __device__ __forceinline__ void finish_row(const FinishParams& p, int64_t r, Fin
         if (out_phys) out_phys[i] = map_phys(row_pt, raw);
       }
     }
-    return;  // the merge's short rows are finish_rows_team_kernel's
+    return;  // the merge's short rows are team_rows'
   }
   if constexpr (!DENSE) {
-    if (p.blocks[p.row_block[r]].n_units == 1) return;  // finish_rows_team_kernel's
+    if (p.blocks[p.row_block[r]].n_units == 1) return;  // team_rows'
   }
 
   if (tid == 0) {
@@ -394,18 +403,45 @@ __device__ __forceinline__ void finish_row(const FinishParams& p, int64_t r, Fin
   sort_emit<TOPK>(buf, tid, row_pt, out_raw, out_phys);
 }
 
-// Rows strided over the grid; the status is read once per row by one thread
-// so that the CTA's threads agree on it.
+// Rows r = blk, blk + nblk, ...; the status is read once per row by one
+// thread so that the CTA's threads agree on it.
 template <int TOPK, bool DENSE>
-__global__ void __launch_bounds__(kFinThreads) finish_kernel(FinishParams p) {
-  __shared__ __align__(16) FinSmem sm;
-  for (int64_t r = blockIdx.x; r < p.rows; r += gridDim.x) {
+__device__ __forceinline__ void merge_rows(const FinishParams& p, int64_t blk, int64_t nblk,
+                                           FinSmem& sm) {
+  for (int64_t r = blk; r < p.rows; r += nblk) {
     if (threadIdx.x == 0) sm.ok = read_status(p.hdr) == kOk;
     __syncthreads();
     if (!sm.ok) return;
     finish_row<TOPK, DENSE>(p, r, sm);
     __syncthreads();  // the row's shared state is free again
   }
+}
+
+// Exact TopK of the rows of a materialised score matrix (the dense path).
+template <int TOPK, bool DENSE>
+__global__ void __launch_bounds__(kFinThreads) finish_kernel(FinishParams p) {
+  __shared__ __align__(16) FinSmem sm;
+  merge_rows<TOPK, DENSE>(p, blockIdx.x, gridDim.x, sm);
+}
+
+// The fused path's finishing step in one launch: CTAs [0, team_blocks) sort
+// the single-unit and short rows (team_rows), the others merge the rows of
+// multi-unit blocks; the two sets of rows are disjoint, so both run at once.
+template <int TOPK>
+union FinishShared {
+  TeamSmem<TOPK> team;
+  FinSmem merge;
+};
+
+template <int TOPK>
+__global__ void __launch_bounds__(kFinThreads) finish_fused_kernel(FinishParams p, int team_blocks) {
+  static_assert(kTeamThreads == kFinThreads, "one block shape for both paths");
+  __shared__ __align__(16) FinishShared<TOPK> sh;
+  if ((int)blockIdx.x < team_blocks)
+    team_rows<TOPK>(p, blockIdx.x, sh.team);
+  else
+    merge_rows<TOPK, false>(p, (int64_t)blockIdx.x - team_blocks, (int64_t)gridDim.x - team_blocks,
+                            sh.merge);
 }
 
 // Row windows of a bare score matrix: 0 <= start <= end <= width.
@@ -420,13 +456,14 @@ __global__ void validate_windows_kernel(const int32_t* row_start, const int32_t*
 
 template <int TOPK, bool DENSE>
 cudaError_t launch_t(const FinishParams& p, cudaStream_t stream) {
-  if (!DENSE) {
-    constexpr int kTeams = kTeamThreads / 32 / (TOPK / kTeamKeys);
-    const int grid = (p.rows + kTeams - 1) / kTeams;
-    finish_rows_team_kernel<TOPK><<<grid, kTeamThreads, 0, stream>>>(p);
+  const int merge_grid = p.rows < kFinGridCap ? p.rows : kFinGridCap;
+  if (DENSE) {
+    finish_kernel<TOPK, DENSE><<<merge_grid, kFinThreads, 0, stream>>>(p);
+  } else {
+    constexpr int kTeams = TeamSmem<TOPK>::kTeams;
+    const int team_grid = (p.rows + kTeams - 1) / kTeams;
+    finish_fused_kernel<TOPK><<<team_grid + merge_grid, kFinThreads, 0, stream>>>(p, team_grid);
   }
-  const int grid = p.rows < kFinGridCap ? p.rows : kFinGridCap;
-  finish_kernel<TOPK, DENSE><<<grid, kFinThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
