@@ -162,9 +162,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   // 4. units per block and candidate row-slots (blocks handled in tiles of
   //    kPlanThreads with a running carry)
   __shared__ int64_t s_unit_carry, s_slot_carry;
+  __shared__ int32_t s_len_min, s_len_max;  // unit lengths in tiles
   if (tid == 0) {
     s_unit_carry = 0;
     s_slot_carry = 0;
+    s_len_min = INT32_MAX;
+    s_len_max = 0;
   }
   __syncthreads();
   for (int64_t base = 0; base < n_blocks; base += kPlanThreads) {
@@ -188,6 +191,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
         bi.unit_first = (int32_t)u_first;
         bi.slot0 = s_first;
         p.blocks[b] = bi;
+        int32_t lmin = INT32_MAX, lmax = 0;
         for (int64_t k = 0; k < nu; ++k) {
           UnitInfo u;
           u.block = (int32_t)b;
@@ -195,6 +199,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
           u.t_begin = bi.tile0 + (int32_t)((k * bi.ntiles) / nu);
           u.t_end = bi.tile0 + (int32_t)(((k + 1) * bi.ntiles) / nu);
           p.units[u_first + k] = u;
+          lmin = min(lmin, u.t_end - u.t_begin);
+          lmax = max(lmax, u.t_end - u.t_begin);
+        }
+        if (nu > 0) {
+          atomicMin(&s_len_min, lmin);
+          atomicMax(&s_len_max, lmax);
         }
       }
     }
@@ -210,8 +220,14 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
 
   // 5. schedule: longest units first (the scorer deals them to its persistent
   //    CTAs band by band, alternating the direction).  With no more units than
-  //    CTAs every unit starts at once and the order cannot matter.
-  if (n_units > p.grid && n_units <= kSortMax) {
+  //    CTAs every unit starts at once and the order cannot matter.  Units of
+  //    nearly equal length (longest <= 1.25 x shortest) are not sorted: the
+  //    alternating deal balances them in any order, and they are dealt last
+  //    block first (a request's later rows have the longer causal windows, so
+  //    this is close to longest first and keeps the short ones for the last,
+  //    partial band).
+  const bool spread = 4ll * s_len_max > 5ll * s_len_min;
+  if (n_units > p.grid && n_units <= kSortMax && spread) {
     int64_t n2 = 1;
     while (n2 < n_units) n2 <<= 1;
     for (int64_t i = tid; i < n2; i += kPlanThreads) {
@@ -240,6 +256,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     }
     for (int64_t i = tid; i < n_units; i += kPlanThreads)
       p.sched[i] = (int32_t)(~(uint32_t)(s_sort[i] & 0xffffffffu));
+  } else if (n_units > p.grid) {
+    for (int64_t i = tid; i < n_units; i += kPlanThreads) p.sched[i] = (int32_t)(n_units - 1 - i);
   } else {
     for (int64_t i = tid; i < n_units; i += kPlanThreads) p.sched[i] = (int32_t)i;
   }
