@@ -159,12 +159,27 @@ def test_runs_on_caller_stream(base):
 
 
 def test_scratch_is_context_independent():
+    # the workspace the query reports for (rows, topk) -- it takes no context
+    # argument -- serves the stream-ordered call at contexts 16x apart
+    import torch
     import fp4_sparse_attention_tma_gb300 as m
-    a = m.idx_topk_fp4_scratch_bytes(8192, 1024)
-    # same rows/topk, any context: the query has no context argument at all;
-    # compare the real pool high-water mark of two calls with 8x different context
-    assert a > 0
-    assert m.idx_topk_fp4_scratch_bytes(1024, 1024) < a
+    rows, K = 48, 512
+    need = m.idx_topk_fp4_scratch_bytes(rows, K)
+    assert 0 < m.idx_topk_fp4_scratch_bytes(8, K) < need
+    for L in (4096, 65536):
+        p = inputs.make_problem(53, [L], [[(0, L - rows + 1 + i) for i in range(rows)]], topk=K)
+        d = H.to_device(p)
+        _, want_phys, want_raw = _call(p, d, K)
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        st = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+        phys = torch.zeros((rows, K), dtype=torch.int32, device="cuda")
+        raw = torch.zeros((rows, K), dtype=torch.int32, device="cuda")
+        code = m.idx_topk_fp4_prefill_async(**d, topk=K, out_phys_slot=phys, out_raw_idx=raw,
+                                            workspace=ws, status=st)
+        torch.cuda.synchronize()
+        assert code == 0 and int(st.item()) == 0
+        assert np.array_equal(phys.cpu().numpy(), want_phys)
+        assert np.array_equal(raw.cpu().numpy(), want_raw)
 
 
 def test_repeated_calls_are_deterministic(base):

@@ -88,8 +88,24 @@ def check_exact_topk_on_device(p, sc, g_raw, g_phys, chunk=256):
 
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4])
 def test_full_size_workload(cfg):
+    check_workload(inputs.config(cfg))
+
+
+def test_more_units_than_the_planner_sorts():
+    # 28,000 rows in 4 requests of 8,192 C4 positions: 9,336 row blocks, each one
+    # work unit of its own length (5 to 64 tiles) -- more units than the planner
+    # sorts, so they are dealt unsorted; random windows, some of them short
+    rng = np.random.default_rng(77)
+    wins = []
+    for _ in range(4):
+        start = rng.integers(0, 4000, size=7000)
+        length = rng.integers(100, 4000, size=7000)
+        wins.append([(int(a), int(a + b)) for a, b in zip(start, length)])
+    check_workload(inputs.make_problem(77, [8192] * 4, wins, topk=512, name="units-9336-K512"))
+
+
+def check_workload(p):
     import torch
-    p = inputs.config(cfg)
     d = H.to_device(p)
     code, g_phys, g_raw = H.run_fused(p, d)
     assert code == 0
