@@ -176,11 +176,18 @@ __device__ __forceinline__ float2 unpack2(uint64_t v) {
   return make_float2(__uint_as_float((uint32_t)v), __uint_as_float((uint32_t)(v >> 32)));
 }
 
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// The four packed partial sums folded lane-wise ((acc0 + acc1) + (acc2 + acc3)),
+// then the two lanes added: three packed adds and one scalar add.
 __device__ __forceinline__ float head_sum_final(const uint64_t (&acc)[4]) {
-  const float2 a0 = unpack2(acc[0]), a1 = unpack2(acc[1]), b0 = unpack2(acc[2]),
-               b1 = unpack2(acc[3]);
+  const float2 t = unpack2(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])));
   // + 0 turns an all-zero total of -0 into +0, the value a sum started at +0 has
-  return (((a0.x + a0.y) + (a1.x + a1.y)) + ((b0.x + b0.y) + (b1.x + b1.y))) + 0.0f;
+  return (t.x + t.y) + 0.0f;
 }
 
 // Collective over a row's four epilogue warps (named barrier bar_id, 128
