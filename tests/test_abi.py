@@ -73,3 +73,47 @@ def test_pages_memory_geometry():
     rows = [l.split() for l in open(path) if l.strip() and not l.startswith("#")]
     for r, ctx, mib in rows:
         assert m.dense_score_bytes(int(r), int(ctx)) / 2**20 == pytest.approx(float(mib))
+
+
+def test_header_is_plain_c_and_links(tmp_path):
+    """include/idxtopk.h compiles as strict C99 and a C program linked against the
+    in-tree library calls the host-only entry points through it."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    lib_path = _lib.build()
+    src = tmp_path / "abi_c.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "idxtopk.h"
+
+int main(void) {
+  const int32_t* ks = NULL;
+  int32_t n = 0;
+  if (idx_topk_supported_k(&ks, &n) != IDX_OK || n != 2 || ks[0] != 512 || ks[1] != 1024)
+    return 1;
+  if (strcmp(idx_topk_status_string(IDX_OK), idx_topk_status_string(IDX_ERR_INVALID_PAGE)) == 0)
+    return 2;
+  /* a null output descriptor fails before any device work */
+  if (idx_topk_fp4_prefill(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 512, NULL, NULL,
+                           (idx_stream_t)0) != IDX_ERR_INVALID_ARGUMENT)
+    return 3;
+  idx_tensor_t t;
+  memset(&t, 0, sizeof(t));
+  t.dtype = IDX_I32;
+  printf("ok %d %zu\n", (int)n, sizeof(t));
+  return 0;
+}
+''')
+    exe = tmp_path / "abi_c"
+    lib_dir = os.path.dirname(lib_path)
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                        "-L", lib_dir, "-l:" + os.path.basename(lib_path),
+                        "-Wl,-rpath," + lib_dir], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    assert r.stdout.split()[:2] == ["ok", "2"]
