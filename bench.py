@@ -208,7 +208,7 @@ def run_reference(args):
     oracle.prefill_rows(p, rows=scored[-1:].astype(np.int32))
     t_row = max(time.perf_counter() - t0, 1e-3)
     budget = 150.0
-    per_step = int(max(1, min(64, budget / (args.steps + args.warmup) / t_row)))
+    per_step = int(max(1, min(64, len(scored), budget / (args.steps + args.warmup) / t_row)))
     rng = np.random.default_rng(0)
     times, flops = [], []
     for i in range(args.warmup + args.steps):

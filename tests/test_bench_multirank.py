@@ -1,6 +1,7 @@
 """Multi-rank logic of bench.py on CPU: two gloo ranks, each with its own step
 time, agree on the slowest rank's time and report the whole-job throughput of
-N replicas of the workload (rows are independent; no data-path collective)."""
+N replicas of the workload (rows are independent; no data-path collective).
+The reference arm (the oracle) prints its line on rank 0 only."""
 import os
 import socket
 
@@ -50,3 +51,38 @@ def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.whole_job_tflops(1e12, 1, 1.0) == pytest.approx(1000.0)
+
+
+def _run_bench(args, env_extra):
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, **env_extra)
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py")] + args, cwd=root, env=env,
+                       capture_output=True, text=True, timeout=300)
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    return r.returncode, [json.loads(l) for l in lines], r.stderr
+
+
+def test_reference_arm_prints_one_line_on_rank_zero():
+    """The reference arm (the oracle on the host cores) on the smallest workload,
+    whose 30 scored rows are fewer than the arm's per-step sample cap."""
+    import bench
+    code, lines, err = _run_bench(["--impl", "reference", "--config", "0", "--steps", "2",
+                                   "--warmup", "3"], {"RANK": "0", "WORLD_SIZE": "1"})
+    assert code == 0, err
+    assert len(lines) == 1
+    d = lines[0]
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s"
+    assert d["steps"] == 2 and d["warmup"] == 3 and d["higher_is_better"] is True
+    assert d["config"]["workload"] == "tiny-R32-S4096-K512" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    code, lines, err = _run_bench(["--impl", "reference", "--config", "0", "--steps", "1",
+                                   "--warmup", "3"], {"RANK": "1", "WORLD_SIZE": "2"})
+    assert code == 0, err
+    assert lines == []
