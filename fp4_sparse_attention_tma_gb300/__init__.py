@@ -26,7 +26,7 @@ __all__ = ["IdxError", "SUPPORTED_K", "idx_topk_fp4_prefill", "idx_topk_fp4_pref
            "idx_fp4_debug_scores", "idx_topk_select_scores", "idx_topk_supported_k",
            "idx_topk_status_string", "idx_topk_fp4_scratch_bytes", "idx_topk_scratch_high_water",
            "dense_score_bytes", "STATUS", "idx_topk_set_timing",
-           "idx_topk_last_timings"]
+           "idx_topk_last_timings", "idx_debug_bounded_wait"]
 
 STATUS = {0: "OK", 1: "INVALID_ARGUMENT", 2: "UNSUPPORTED", 3: "INVALID_METADATA",
           4: "INVALID_PAGE", 5: "OVERFLOW", 6: "CUDA_ERROR", 7: "INTERNAL", 8: "TIMEOUT",
@@ -217,6 +217,13 @@ def idx_topk_scratch_high_water(device: int = 0) -> int:
     code = _lib.load().idx_topk_scratch_high_water(int(device), ctypes.byref(v))
     _check(code, "idx_topk_scratch_high_water", True)
     return int(v.value)
+
+
+def idx_debug_bounded_wait(never_completes: bool, device: int = 0, stream=None) -> int:
+    """Failure-detection diagnostic: the status a bounded device wait records
+    (0, or IDX_ERR_TIMEOUT = 8 after its 2 s limit when nothing completes it)."""
+    return int(_lib.load().idx_debug_bounded_wait(int(device), 1 if never_completes else 0,
+                                                  _stream(stream)))
 
 
 def idx_topk_set_timing(enable: bool) -> None:

@@ -108,6 +108,7 @@ EXPORTS = {
     "idx_topk_fp4_scratch_bytes": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                   ctypes.POINTER(ctypes.c_uint64)]),
     "idx_topk_scratch_high_water": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(ctypes.c_uint64)]),
+    "idx_debug_bounded_wait": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]),
     "idx_topk_set_timing": (ctypes.c_int, [ctypes.c_int32]),
     "idx_topk_last_timings": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float)]),
 }

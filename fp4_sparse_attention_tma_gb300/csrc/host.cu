@@ -1350,6 +1350,29 @@ int idx_topk_last_timings(float* ms4) {
   return IDX_OK;
 }
 
+int idx_debug_bounded_wait(int32_t device, int32_t never_completes, idx_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  DeviceState* ds = nullptr;
+  int st = device_state(device, &ds);
+  if (st) return st;
+  DeviceGuard guard(device);
+  if (!guard.ok()) return IDX_ERR_CUDA;
+  if ((st = check_stream(stream, device))) return st;
+  Scratch s;
+  s.L.header = 0;
+  s.L.total = align_up(sizeof(PlanHeader), 256);
+  if (cudaMallocFromPoolAsync(&s.base, s.L.total, ds->pool, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return IDX_ERR_CUDA;
+  }
+  cudaMemsetAsync(s.hdr(), 0, sizeof(PlanHeader), stream);
+  const bool launch_err = launch_wait_probe(s.hdr(), never_completes != 0, stream) != cudaSuccess;
+  uint32_t status = kOk;
+  st = read_status_and_free(s, stream, &status);
+  if (launch_err || st || cudaGetLastError() != cudaSuccess) return IDX_ERR_CUDA;
+  return (int)status;
+}
+
 int idx_topk_scratch_high_water(int32_t device, uint64_t* bytes) {
   if (!bytes) return IDX_ERR_INVALID_ARGUMENT;
   DeviceState* ds = nullptr;

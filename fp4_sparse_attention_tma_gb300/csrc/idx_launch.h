@@ -22,6 +22,11 @@ inline cudaError_t set_smem_once(Kernel kernel, int bytes, bool (&done)[64]) {
   return err;
 }
 
+// One CTA waiting through the bounded mbarrier wait on a phase that its own
+// thread completes (never = false) or that nothing completes (never = true:
+// kErrTimeout is recorded in hdr after the wait limit).
+cudaError_t launch_wait_probe(PlanHeader* hdr, bool never, cudaStream_t stream);
+
 // plan_kernel (1 CTA) then validate_pages_kernel.
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 

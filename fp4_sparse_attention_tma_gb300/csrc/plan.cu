@@ -320,7 +320,32 @@ __global__ void __launch_bounds__(256) validate_pages_kernel(PlanParams p) {
   }
 }
 
+// Failure-detection diagnostic: one CTA waits through the bounded mbarrier
+// wait that every kernel of the library uses.  The phase is completed by the
+// CTA's own thread 0 (never == 0), or by nothing (never != 0): the wait then
+// gives up after its time limit, records kErrTimeout and the kernel returns.
+// Nothing else is in flight, so the context stays usable.
+__global__ void __launch_bounds__(64) wait_probe_kernel(PlanHeader* hdr, int never) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (!never && threadIdx.x == 0) mbar_arrive(b);
+  if (threadIdx.x < 32) mbar_wait(b, 0, &abort_flag, hdr, 900);
+  __syncthreads();
+}
+
 }  // namespace
+
+cudaError_t launch_wait_probe(PlanHeader* hdr, bool never, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 64, 0, stream>>>(hdr, never ? 1 : 0);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
   static const size_t kSortBytes = sizeof(uint64_t) * kSortMax;

@@ -249,6 +249,18 @@ const char* idx_topk_status_string(int code);
  * IDX_ERR_CUDA if the device cannot be queried. */
 int idx_topk_fp4_scratch_bytes(int32_t rows, int32_t topk, int32_t device, uint64_t* bytes);
 
+/* Diagnostic of the device-side failure detection (no counterpart on the
+ * pages).  One CTA on `device` waits, through the same bounded mbarrier wait
+ * every kernel of the library uses, on a phase that its own thread completes
+ * (never_completes == 0) or that nothing completes (never_completes != 0).
+ * Returns the status the kernel recorded: IDX_OK, or IDX_ERR_TIMEOUT once the
+ * wait has given up after its 2 s limit -- the kernel then returns with
+ * nothing in flight and the CUDA context stays usable.  Synchronises
+ * `stream`; IDX_ERR_UNSUPPORTED while the stream is being captured;
+ * IDX_ERR_INVALID_ARGUMENT for a bad device index or a stream of another
+ * device. */
+int idx_debug_bounded_wait(int32_t device, int32_t never_completes, idx_stream_t stream);
+
 /* Peak bytes ever reserved by the library's scratch pool on `device` in this
  * process (the pool's reserved-memory high-water mark). */
 int idx_topk_scratch_high_water(int32_t device, uint64_t* bytes);

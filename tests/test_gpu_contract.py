@@ -187,3 +187,19 @@ def test_repeated_calls_are_deterministic(base):
     r1 = _call(base, d)
     r2 = _call(base, d)
     assert np.array_equal(r1[1], r2[1]) and np.array_equal(r1[2], r2[2])
+
+
+def test_expired_device_wait_returns_a_status_and_the_context_stays_usable(base):
+    # a bounded mbarrier wait on a phase that nothing completes gives up after
+    # its 2 s limit and the kernel records IDX_ERR_TIMEOUT instead of hanging;
+    # the same wait completes normally when the phase is completed, and a
+    # regular call afterwards still succeeds on the same context
+    import time
+    import fp4_sparse_attention_tma_gb300 as m
+    assert m.idx_debug_bounded_wait(False) == 0
+    t0 = time.perf_counter()
+    assert m.idx_debug_bounded_wait(True) == 8
+    assert 1.9 < time.perf_counter() - t0 < 60
+    assert m.idx_debug_bounded_wait(False) == 0
+    code, _, raw = _call(base, H.to_device(base))
+    assert code == 0 and (raw >= 0).any()
