@@ -305,10 +305,10 @@ struct UnitView {
   BlockInfo b;
 };
 
-// Schedule position of this CTA's i-th unit.  The units are sorted longest
-// first; band i (positions i*G .. i*G+G-1) is dealt to the CTAs in ascending
-// order when i is even and descending when odd, so a CTA that drew a longer
-// unit of one band draws a shorter one of the next.
+// Schedule position of this CTA's i-th unit.  The planner orders the units
+// longest first (or nearly so); band i (positions i*G .. i*G+G-1) is dealt in
+// ascending CTA order when i is even and descending when odd, so a CTA that
+// drew a longer unit of one band draws a shorter one of the next.
 __device__ __forceinline__ int cta_unit(int i) {
   const int c = (i & 1) ? (int)(gridDim.x - 1u - blockIdx.x) : (int)blockIdx.x;
   return i * (int)gridDim.x + c;
