@@ -33,6 +33,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fused score+TopK ms & FP4 TFLOPS (% peak) at Q=8192, C4=196608, K=1024"
+# The pages' own fused-path times for two of the workloads (Q=8192 rows, MI355X;
+# "[FlyDSL] Add FP4 LiteTopK prefill operator", Validation table): another
+# machine's numbers, the denominator of vs_baseline, not targets.
+PAGES_MS = {"pro-R8192-S196608-K1024": 10.6433,    # V4-Pro, K=1024, C4 196,608
+            "flash-R8192-S131072-K512": 7.2235}    # V4-Flash, K=512, C4 131,072
 NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense FP4 : bf16 tensor ratio of GB300
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
@@ -63,6 +68,15 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def vs_baseline(workload: str, flop: float, value_tflops: float):
+    """value / the pages' throughput on the same workload (the same algorithmic
+    FLOP over the pages' time), or None where the pages give no time for it."""
+    ms = PAGES_MS.get(workload)
+    if ms is None:
+        return None
+    return value_tflops / (flop / (ms * 1e-3) / 1e12)
 
 
 def max_over_ranks(x: float, world: int, device=None) -> float:
@@ -224,7 +238,8 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": vs_baseline(p.name, float(p.algorithmic_flop()), value),
+            "dtype": "f64", "data": "synthetic",
             "config": {"workload": p.name, "rows": p.rows, "c4_context": p.max_end(),
                        "topk": p.topk},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(),
@@ -323,7 +338,8 @@ def main():
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp4",
+            "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": vs_baseline(p.name, flop, value), "dtype": "fp4",
             "data": "synthetic",
             "config": {"workload": p.name, "rows": R, "c4_context": p.max_end(), "topk": K,
                        "heads": 64, "dim": 128, "page": 64, "scored_pairs": p.scored_pairs(),

@@ -79,6 +79,7 @@ def test_reference_arm_prints_one_line_on_rank_zero():
     assert d["config"]["workload"] == "tiny-R32-S4096-K512" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["vs_baseline"] is None          # the pages give no time for this workload
 
 
 def test_reference_arm_other_ranks_exit_without_work():
@@ -86,3 +87,15 @@ def test_reference_arm_other_ranks_exit_without_work():
                                    "--warmup", "3"], {"RANK": "1", "WORLD_SIZE": "2"})
     assert code == 0, err
     assert lines == []
+
+
+def test_vs_baseline_divides_by_the_pages_throughput_on_the_same_workload():
+    import bench
+    flop = 2.6251e13
+    # the pages' fused-path time on this workload (MI355X): 10.6433 ms
+    same = flop / 10.6433e-3 / 1e12
+    assert bench.vs_baseline("pro-R8192-S196608-K1024", flop, same) == pytest.approx(1.0)
+    assert bench.vs_baseline("pro-R8192-S196608-K1024", flop, same / 2) == pytest.approx(0.5)
+    assert bench.vs_baseline("flash-R8192-S131072-K512", 1.7455e13,
+                             1.7455e13 / 7.2235e-3 / 1e12) == pytest.approx(1.0)
+    assert bench.vs_baseline("mid-R1024-4req-8k..64k-K512", 5.15e11, 1.0) is None
