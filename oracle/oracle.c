@@ -19,8 +19,8 @@
  *                  the window is not longer than topk (short-row contract,
  *                  aiter#5282 Changes);
  *   out_phys[r]  = page_table[req][raw / 64] * 64 + raw % 64, -1 stays -1
- *                  (aiter#5282 Changes: "map raw C4 positions through the page
- *                  table").
+ *                  (aiter#5282 Changes: the raw C4 positions become physical
+ *                  slots through the page table).
  *
  * Data formats: E2M1 as in the OCP Microscaling Formats (MX) v1.0 spec
  * (1 sign, 2 exponent bits with bias 1, 1 mantissa bit), two codes per byte

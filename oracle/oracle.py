@@ -42,7 +42,9 @@ def _load():
     with _lock:
         if _lib is not None:
             return _lib
-        lib = ctypes.CDLL(build())
+        # a prebuilt variant of the library (the pin-strength test loads copies of
+        # oracle.c with one planted mistake each through this variable)
+        lib = ctypes.CDLL(os.environ.get("IDXTOPK_ORACLE_LIB") or build())
         P = ctypes.c_void_p
         i32, i64 = ctypes.c_int32, ctypes.c_int64
         lib.oracle_threads.restype = ctypes.c_int
