@@ -107,7 +107,9 @@ typedef struct {
  *   out_raw_idx   i32 [R, topk]    logical C4 position or -1; may be NULL
  *
  * Rows whose window is longer than topk are ordered by (score desc, position asc).
- * Scale bytes of 255 (NaN) are outside the contract.
+ * Scale bytes of 255 (NaN) are outside the contract.  The operation is the one
+ * defined at the top of this file (aiter#5309 Summary and Implementation;
+ * aiter#5282 Changes and Scope).
  */
 int idx_topk_fp4_prefill(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
                          const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
@@ -136,8 +138,8 @@ int idx_topk_fp4_prefill_paged(const idx_tensor_t* q_fp4, const idx_tensor_t* q_
                                const idx_tensor_t* out_raw_idx, idx_stream_t stream);
 
 /*
- * idx_topk_fp4_prefill on tensors in host memory (the pages have no
- * counterpart: it serves callers whose query block, K cache and metadata sit
+ * idx_topk_fp4_prefill on tensors in host memory (no counterpart on the
+ * pages: it serves callers whose query block, K cache and metadata sit
  * in host memory, and it is the end-to-end form of the operation, host copies
  * included).
  *   device  the GPU to run on (0 .. count-1); stream must belong to it or be NULL.
@@ -200,8 +202,8 @@ int idx_topk_fp4_prefill_async(const idx_tensor_t* q_fp4, const idx_tensor_t* q_
                                idx_stream_t stream);
 
 /*
- * Allocation-free variant of idx_topk_fp4_prefill (the pages have no
- * counterpart; it exists for callers that must not allocate device memory
+ * Allocation-free variant of idx_topk_fp4_prefill (no counterpart on the
+ * pages; it exists for callers that must not allocate device memory
  * during a call: a serving process that has handed all free HBM to its own
  * caches and allocator, so a new reservation would fail or evict; or a caller
  * that cannot afford the device synchronisation and driver work that growing
@@ -239,7 +241,8 @@ int idx_topk_fp4_prefill_noalloc(const idx_tensor_t* q_fp4, const idx_tensor_t* 
  * an argument is NULL (IDX_ERR_INVALID_ARGUMENT). */
 int idx_topk_supported_k(const int32_t** ks, int32_t* n);
 
-/* Static, human-readable name of a status code. */
+/* Static, human-readable name of a status code (the fail-closed status
+ * contract of aiter#5309 Implementation). */
 const char* idx_topk_status_string(int code);
 
 /* Scratch bytes that idx_topk_fp4_prefill allocates for `rows` rows and
@@ -262,7 +265,9 @@ int idx_topk_fp4_scratch_bytes(int32_t rows, int32_t topk, int32_t device, uint6
 int idx_debug_bounded_wait(int32_t device, int32_t never_completes, idx_stream_t stream);
 
 /* Peak bytes ever reserved by the library's scratch pool on `device` in this
- * process (the pool's reserved-memory high-water mark). */
+ * process (the pool's reserved-memory high-water mark).  Measurement support
+ * with no counterpart on the pages; it evidences the context-independent
+ * scratch bound of aiter#5282 Changes. */
 int idx_topk_scratch_high_water(int32_t device, uint64_t* bytes);
 
 /* Measurement support (no counterpart on the pages): when enabled, each call
@@ -295,7 +300,8 @@ int idx_tiled_topk_fp4_prefill(const idx_tensor_t* q_fp4, const idx_tensor_t* q_
 
 /*
  * Debug / dense scorer: the same scoring kernel as the fused path, writing the
- * fp32 scores instead of selecting.
+ * fp32 scores instead of selecting (no counterpart on the pages; it exposes
+ * the scores and per-head logits that the parity tests compare).
  *   out_scores f32 [R, S]      score[r, s] written for every s in [start_r, end_r)
  *                              of every row with a non-empty window; other entries are
  *                              left untouched.  S >= max(row_end) is required and
@@ -313,8 +319,10 @@ int idx_fp4_debug_scores(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
 
 /*
  * Exact TopK of a materialised fp32 score matrix under the same total order and
- * short-row contract (the selection half of the dense comparison path; also the
- * entry that pins NaN / signed-zero / tie ordering on crafted matrices).
+ * short-row contract (aiter#5282 Changes: the order key, NaN below every
+ * number, +0 above -0, ties to the lower position; the selection half of the
+ * dense comparison path, and the entry that pins that ordering on crafted
+ * matrices).
  *   scores      f32 [R, S]   row r's candidates are scores[r, start_r .. end_r)
  *   row_start, row_end i32 [R]
  *   out_raw_idx i32 [R, topk]   positions (absolute within the row) or -1
@@ -326,7 +334,9 @@ int idx_topk_select_scores(const idx_tensor_t* scores, const idx_tensor_t* row_s
 
 /*
  * Dense comparison path: materialises fp32 scores [R, score_stride] (rows with
- * window longer than topk), then runs the separate TopK and the page mapping.
+ * window longer than topk), then runs the separate TopK and the page mapping
+ * (aiter#5309 Validation: the dense-scores-then-TopK baseline the pages time
+ * the fused operator against).
  * Same arguments and outputs as idx_topk_fp4_prefill plus:
  *   score_workspace f32 [R, S_ws], S_ws >= max(row_end), caller-owned; may be
  *                   NULL, in which case R * MP * 64 * 4 bytes are allocated

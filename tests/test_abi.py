@@ -117,3 +117,14 @@ int main(void) {
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
     assert r.stdout.split()[:2] == ["ok", "2"]
+
+
+def test_every_declaration_cites_its_passage():
+    """Each entry point's comment cites the passage that defines it, or says that
+    the pages have no counterpart."""
+    text = open(HEADER).read()
+    for m in re.finditer(r"^(?:int|const char\*)\s+(idx_\w+)\s*\(", text, re.M):
+        before = text[:m.start()]
+        j = before.rfind("/*")
+        comment = re.sub(r"\s*\n\s*\*\s?", " ", before[j:before.rfind("*/")])
+        assert re.search(r"aiter#\d+|sglang#\d+|no counterpart on the pages", comment), m.group(1)
