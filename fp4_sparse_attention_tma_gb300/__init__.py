@@ -136,7 +136,9 @@ def idx_topk_fp4_prefill_noalloc(q_fp4, q_scale, k_cache_fp4, k_scale, weights, 
                                  row_req, row_start, row_end, topk, out_phys_slot, out_raw_idx=None,
                                  stream=None, raise_on_error=True) -> int:
     """idx_topk_fp4_prefill with its scratch in the library's fixed per-device
-    buffer: allocates nothing; overlapping calls on one device race."""
+    buffer: allocates no device memory.  Calls on one device are serialised by
+    a per-device lock held until the call's work has completed, so they never
+    overlap on the buffer; the call returns after its stream has finished."""
     lib = _lib.load()
     ds = [_desc(t) for t in (q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
                              row_start, row_end, out_phys_slot, out_raw_idx)]

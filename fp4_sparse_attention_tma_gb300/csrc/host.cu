@@ -620,12 +620,14 @@ int run_fixed_scratch(const Call& c, cudaStream_t stream) {
                                c.out_raw};
   int dev = -1;
   if ((st = common_device(all, 11, &dev))) return st;
+  // the per-device lock and buffer tables are indexed by dev
+  if (dev < 0 || dev >= kMaxDevices) return IDX_ERR_INVALID_ARGUMENT;
   DeviceGuard guard(dev);
   if (!guard.ok()) return IDX_ERR_CUDA;
   st = check_stream(stream, dev);
   if (st == IDX_ERR_UNSUPPORTED) return st;  // capturing: enqueue nothing
   auto fail = [&](int code) {
-    fill_minus_one(outs, stream);
+    fill_minus_one(outs, stream);  // also waits for the stream
     return code;
   };
   if (st) return fail(st);
@@ -722,7 +724,13 @@ int run_fixed_scratch(const Call& c, cudaStream_t stream) {
   if (cudaMemcpyAsync(&status, s.hdr(), sizeof(uint32_t), cudaMemcpyDeviceToHost, stream) !=
       cudaSuccess)
     cuda_err = 1;
-  if (cuda_err || cudaGetLastError() != cudaSuccess) return fail(IDX_ERR_CUDA);
+  if (cuda_err || cudaGetLastError() != cudaSuccess) {
+    // a launch or the read-back failed: wait until every kernel that was
+    // enqueued has finished with the shared buffer before the lock is released
+    cudaStreamSynchronize(stream);
+    cudaGetLastError();
+    return fail(IDX_ERR_CUDA);
+  }
   if (status != kOk) return fail((int)status);
   return IDX_OK;
 }

@@ -5,20 +5,25 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "idx_internal.h"
 
 namespace idxk {
 
 // Sets a kernel's dynamic shared-memory limit once per device (the attribute
 // persists, and repeating the call is avoided while a stream is captured).
+// Host threads may call at once: the per-device flags are atomic, and two
+// threads that both see a flag clear both set the same attribute, which is
+// harmless.
 template <typename Kernel>
-inline cudaError_t set_smem_once(Kernel kernel, int bytes, bool (&done)[64]) {
+inline cudaError_t set_smem_once(Kernel kernel, int bytes, std::atomic<bool> (&done)[64]) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (done[dev]) return cudaSuccess;
+  if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
   const cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (err == cudaSuccess) done[dev] = true;
+  if (err == cudaSuccess) done[dev].store(true, std::memory_order_release);
   return err;
 }
 

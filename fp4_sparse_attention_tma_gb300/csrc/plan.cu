@@ -349,7 +349,7 @@ cudaError_t launch_wait_probe(PlanHeader* hdr, bool never, cudaStream_t stream) 
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
   static const size_t kSortBytes = sizeof(uint64_t) * kSortMax;
-  static bool done[64] = {};
+  static std::atomic<bool> done[64] = {};
   cudaError_t err = set_smem_once(plan_kernel, (int)kSortBytes, done);
   if (err != cudaSuccess) return err;
   plan_kernel<<<1, kPlanThreads, kSortBytes, stream>>>(p);

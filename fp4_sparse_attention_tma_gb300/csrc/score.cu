@@ -793,7 +793,7 @@ template <int MODE, int TOPK>
 cudaError_t launch_score_t(const CUtensorMap& tk, const CUtensorMap& tq, const ScoreParams& p,
                            int grid, cudaStream_t stream) {
   const size_t smem = smem_bytes_for(MODE, TOPK);
-  static bool done[64] = {};
+  static std::atomic<bool> done[64] = {};
   cudaError_t err = set_smem_once(score_kernel<MODE, TOPK>, (int)smem, done);
   if (err != cudaSuccess) return err;
   score_kernel<MODE, TOPK><<<grid, kThreads, smem, stream>>>(tk, tq, p);

@@ -218,9 +218,17 @@ int idx_topk_fp4_prefill_async(const idx_tensor_t* q_fp4, const idx_tensor_t* q_
  * returns IDX_ERR_SCRATCH_LIMIT (outputs filled with -1) without running.
  * At 152 SMs that admits up to about 5,640 rows at topk 1024 and 11,630 at 512.
  *
- *  - The first call on a device looks up the buffer's address there (the
- *    device is made current for it); make that first call before any stream
- *    capture begins.
+ *  - The buffer is reserved on a device when the library's device code is
+ *    loaded there: under CUDA's default lazy module loading that happens at
+ *    the first call of this function on the device (which also looks up the
+ *    buffer's address, with the device made current); under eager loading
+ *    (CUDA_MODULE_LOADING=EAGER) it happens when the process creates its
+ *    context on the device, whether or not this function is ever called.
+ *    Make the first call before any stream capture begins, and before the
+ *    caller hands the device's remaining memory to its own allocator (the
+ *    reservation can fail with IDX_ERR_CUDA when no memory is left).
+ *  - A device index of 64 or more is rejected with IDX_ERR_INVALID_ARGUMENT
+ *    before anything is enqueued.
  *  - All calls on one device share the one buffer.  The call returns only
  *    after its work on `stream` has completed, and a per-device lock held for
  *    the whole call makes concurrent calls from several host threads run one

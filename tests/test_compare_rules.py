@@ -1,7 +1,8 @@
 """The comparison rules the GPU parity tests apply (tests/helpers.py), checked on
 the CPU with crafted rows: identical outputs pass; a selected position whose
 oracle score lies within the tolerance of the K-th score may replace another
-one (counted); any other difference, a wrong physical slot or a wrong short row
+one (counted); any other difference, an order that contradicts the oracle
+scores by more than the tolerance, a wrong physical slot or a wrong short row
 fails; the score bound follows its formula."""
 from types import SimpleNamespace
 
@@ -71,3 +72,39 @@ def test_score_bound_formula():
     w[:3] = [2.0, -3.0, -0.5]
     # 1e-6 + 1e-5 * (|2| * 1 + |-3| * 0 + |-0.5| * 4)
     assert H.score_bound(logits, w)[0] == pytest.approx(1e-6 + 1e-5 * 4.0)
+
+
+def test_same_set_in_wrong_order_fails():
+    # the oracle's set, but scores 3.0 and 2.5 swapped: far outside tolerance
+    with pytest.raises(AssertionError):
+        _cmp(_problem(10), np.array([5, 1, 3, 6]))
+
+
+def test_same_set_order_swap_within_tolerance_passes():
+    # positions 2 (1.0) and 6 (1.0 + 5e-6) lie within 1e-5 relative of each
+    # other: fp32 rounding may order them either way
+    assert _cmp(_problem(10), np.array([1, 5, 3, 2]), o_raw=np.array([1, 5, 3, 6])) == 1
+    assert H.order_follows_oracle(np.array([1, 5, 3, 2, 6]), SCORES, 0)
+    assert H.order_follows_oracle(np.array([1, 5, 3, 6, 2]), SCORES, 0)
+
+
+def test_equal_scores_must_come_in_position_order():
+    sc = np.array([2.0, 1.0, 2.0, 1.0])
+    assert H.order_follows_oracle(np.array([0, 2, 1, 3]), sc, 0)
+    assert not H.order_follows_oracle(np.array([2, 0, 1, 3]), sc, 0)
+
+
+def test_selected_scores_pure_bar_and_counted_waiver():
+    w = np.zeros(64, np.float32)
+    w[:2] = [1.0, -1.0]
+    lg = np.zeros((3, 64))
+    lg[:, 0] = [10.0, 10.0, 10.0]
+    lg[:, 1] = [0.0, 0.0, 9.9999]
+    want = np.array([10.0, 10.0, 1e-4])              # the third sum cancels 2e5-fold
+    # within 1e-5 relative: passes with no waiver
+    assert H.check_selected_scores(want * (1 + 5e-6), want, lg, w) == 0
+    # the cancelling sum off by 1e-5 absolute: within the conditioned bound, waived
+    assert H.check_selected_scores(want + np.array([0, 0, 1e-5]), want, lg, w) == 1
+    # a well-conditioned score off by 2e-5 relative fails
+    with pytest.raises(AssertionError):
+        H.check_selected_scores(want * np.array([1 + 2e-5, 1, 1]), want, lg, w)

@@ -1,9 +1,12 @@
 """Full-size workloads (the four large configurations) in the launch
 configuration the benchmark times.
 
-* Sampled rows (first and last row of every request, two random rows per
-  request, and the special short/empty rows) are compared with the oracle one by
-  one: identical, or differing only at the selection boundary within tolerance.
+* Sampled rows (first and last row of every request, at least 32 random rows
+  spread over the requests, and the special short/empty rows) are compared with
+  the oracle one by one: identical, or differing only at the selection boundary
+  within tolerance; their scores meet the conditioned tolerance over the whole
+  window and the pure rtol/atol bar on the selected positions (waivers for
+  cancelling sums counted).
 * Every row: the selected set is exactly the TopK of the GPU's own scores
   (from the debug dump of the same scoring kernel), checked on the device: each
   selected order key is above every unselected in-window key, the output is in
@@ -21,10 +24,14 @@ from tests import helpers as H
 pytestmark = pytest.mark.gpu
 
 
-def sample_rows(p, per_req=2, seed=0):
+def sample_rows(p, total=32, seed=0):
+    """First and last row of every request, random rows (at least `total` over
+    all requests, spread evenly), and the first short rows."""
     rng = np.random.default_rng(seed)
     rows = set()
-    for req in np.unique(p.row_req):
+    reqs = np.unique(p.row_req)
+    per_req = max(2, -(-total // len(reqs)))
+    for req in reqs:
         idx = np.nonzero(p.row_req == req)[0]
         rows.update([int(idx[0]), int(idx[-1])])
         rows.update(int(x) for x in rng.choice(idx, size=min(per_req, idx.size), replace=False))
@@ -118,15 +125,22 @@ def check_workload(p):
     assert ndiff <= max(2, len(rows) // 4)
     sc, _ = H.run_debug(p, d)
     check_exact_topk_on_device(p, sc, g_raw, g_phys)
-    # GPU scores of the sampled rows against the oracle (conditioned tolerance)
-    for r in rows[:6]:
+    # GPU scores of every sampled row against the oracle: the conditioned
+    # tolerance on the whole window, the pure rtol/atol bar on the selected ones
+    n_sel = n_exempt = 0
+    for r in rows:
         s0, s1 = int(p.row_start[r]), int(p.row_end[r])
         if s1 - s0 <= p.topk:
             continue
-        want = oracle.row_scores(p, int(r))[0]
+        want = scores[int(r)]
         lg, _ = oracle.row_logits(p, int(r), s0, s1)
         got = sc[int(r), s0:s1].double().cpu().numpy()
         assert np.all(np.abs(got - want) <= H.score_bound(lg, p.weights[r])), r
+        sel = g_raw[r] - s0
+        n_exempt += H.check_selected_scores(got[sel], want[sel], lg[sel], p.weights[r])
+        n_sel += sel.size
+    print(f"{p.name}: {len(rows)} rows against the oracle; selected scores outside the "
+          f"pure rtol/atol bar (cancelling sums): {n_exempt} of {n_sel}")
     del sc
     torch.cuda.empty_cache()
     dp, dr = H.run_dense(p, d)

@@ -65,6 +65,7 @@ def test_scores_within_tolerance(p0, small):
 
 
 def test_fused_matches_oracle_and_own_scores(p0, small):
+    n_exempt = n_selected = 0
     for p in (p0, small):
         code, g_phys, g_raw = H.run_fused(p)
         assert code == 0
@@ -82,16 +83,14 @@ def test_fused_matches_oracle_and_own_scores(p0, small):
             want = H.brute_topk(sc[r, s0:s1], p.topk, s0)
             assert np.array_equal(g_raw[r], want), r
             # selected scores: conditioned bound always; pure rtol/atol except
-            # where the head sum cancels by 10x or more
+            # where the head sum cancels by 10x or more (counted)
             sel = g_raw[r] - s0
-            o = oracle.row_scores(p, r)[0][sel]
             lg, _ = oracle.row_logits(p, r, s0, s1)
-            mag = np.maximum(lg[sel], 0.0) @ np.abs(p.weights[r].astype(np.float64))
-            g = sc[r, g_raw[r]].astype(np.float64)
-            err = np.abs(g - o)
-            assert np.all(err <= H.ATOL + H.RTOL * mag), r
-            pure_miss = err > H.ATOL + H.RTOL * np.abs(o)
-            assert np.all(np.abs(o[pure_miss]) * 10 <= mag[pure_miss]), r
+            n_exempt += H.check_selected_scores(sc[r, g_raw[r]], oracle.row_scores(p, r)[0][sel],
+                                                lg[sel], p.weights[r])
+            n_selected += sel.size
+    print(f"selected scores outside the pure rtol/atol bar (cancelling sums): "
+          f"{n_exempt} of {n_selected}")
 
 
 def test_fused_equals_dense_bitwise(p0, small):

@@ -2,7 +2,8 @@
 a copy of oracle/oracle.c -- a dropped or inverted ReLU, a wrong weight index or
 sign, a wrong scale exponent or block, misaligned operands, a wrong E2M1 value, a
 reversed tie, zero-sign or NaN rule, an off-by-one short-row boundary, a page
-table that is ignored, a query row that is ignored -- builds it, and runs
+table that is ignored, a query row that is ignored, an fp32-exactness flag that
+never fires or counts 53 significant bits -- builds it, and runs
 tests/test_oracle_pins.py against it.  Every mutant must fail at least one pin;
 the unmodified copy must pass them all."""
 import os
@@ -38,6 +39,12 @@ MUTANTS = [
     ("short rows only below topk", "if (len <= topk) {", "if (len < topk) {"),
     ("page table ignored", "*phys_row = (int64_t)page * NPAGE + (s % NPAGE);",
      "*phys_row = (int64_t)p * NPAGE + (s % NPAGE);"),
+    ("fp32 exactness flag never set",
+     "if (bits > 24 || m < -149 || m + bits > 128) *f32_exact = 0;",
+     "if (0) *f32_exact = 0;"),
+    ("fp32 significand taken as 53 bits",
+     "if (bits > 24 || m < -149 || m + bits > 128) *f32_exact = 0;",
+     "if (bits > 53 || m < -149 || m + bits > 128) *f32_exact = 0;"),
     ("query row ignored",
      "decode_row(q_fp4 + ((int64_t)row * NH + h) * NDB, q_scale + ((int64_t)row * NH + h) * NSF, &qr[h]);\n"
      "    w[h]",

@@ -129,6 +129,32 @@ def test_generator_keeps_dots_fp32_exact():
     assert inexact == 0
 
 
+def test_inexact_flag_fires_on_a_wide_exponent_span():
+    # Q head 0 and K slot 0: codes 1.0 in blocks 0 and 1, block exponents +15
+    # and 0 on both sides, so the dot is 32 * 2^30 + 32 = 2^5 * (2^30 + 1): 31
+    # significant bits, exact in float64 but not in fp32's 24.  Every other dot
+    # is 0.  The flag must count exactly that one dot, and the value itself must
+    # still be exact.
+    p = inputs.make_problem(2, [64], [[(0, 64)]], 512, page_perm=False)
+    p.q_fp4[:] = 0
+    p.k_cache_fp4[:] = 0
+    p.q_fp4[0, 0, :32] = 0x22
+    p.k_cache_fp4[0, 0, :32] = 0x22
+    p.q_scale[:] = 127
+    p.k_scale[:] = 127
+    p.q_scale[0, 0, 0] = 127 + 15
+    p.k_scale[0, 0, 0] = 127 + 15
+    got, inexact = oracle.row_logits(p, 0, 0, 64)
+    assert inexact == 1
+    assert got[0, 0] == 32.0 * 2.0 ** 30 + 32.0
+    assert np.count_nonzero(got) == 1
+    # a span of 22 keeps the value inside 24 significant bits: exact again
+    p.q_scale[0, 0, 0] = 127 + 11
+    p.k_scale[0, 0, 0] = 127 + 11
+    got, inexact = oracle.row_logits(p, 0, 0, 64)
+    assert inexact == 0 and got[0, 0] == 32.0 * 2.0 ** 22 + 32.0
+
+
 # ---- scores ---------------------------------------------------------------
 
 def _negated_k(p):
