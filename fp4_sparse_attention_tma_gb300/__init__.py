@@ -30,7 +30,7 @@ __all__ = ["IdxError", "SUPPORTED_K", "idx_topk_fp4_prefill", "idx_topk_fp4_pref
 
 STATUS = {0: "OK", 1: "INVALID_ARGUMENT", 2: "UNSUPPORTED", 3: "INVALID_METADATA",
           4: "INVALID_PAGE", 5: "OVERFLOW", 6: "CUDA_ERROR", 7: "INTERNAL", 8: "TIMEOUT",
-          9: "SCRATCH_LIMIT"}
+          9: "SCRATCH_LIMIT", 10: "INVALID_VALUE"}
 SUPPORTED_K = (512, 1024)
 
 _DT = {"uint8": 1, "int32": 2, "float32": 3}

@@ -1331,6 +1331,8 @@ const char* idx_topk_status_string(int code) {
     case IDX_ERR_INTERNAL: return "internal selector failure";
     case IDX_ERR_TIMEOUT: return "device wait timed out";
     case IDX_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the fixed buffer holds";
+    case IDX_ERR_INVALID_VALUE:
+      return "scale byte above 167 or weight not finite or above 2^24 in magnitude";
     default: return "unknown status";
   }
 }

@@ -33,6 +33,20 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // A bounded wait gives up after this long and reports kErrTimeout.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
+// ----------------------------------------------------------- value domain ----
+// Nonzero when some byte of `w` exceeds kMaxScaleByte (167 = 0xA7): a byte b is
+// >= 168 exactly when its top bit is set and (b & 0x7F) + 88 carries into bit 7
+// (no carry crosses bytes, since (b & 0x7F) + 88 <= 0xD7).
+__device__ __forceinline__ uint32_t scale_bytes_over(uint32_t w) {
+  static_assert(kMaxScaleByte == 167, "the byte test below is written for 167");
+  return ((w & 0x7F7F7F7Fu) + 0x58585858u) & w & 0x80808080u;
+}
+
+// True when the fp32 weight with bits `b` is NaN, infinite or above 2^24 in magnitude.
+__device__ __forceinline__ bool weight_out_of_domain(uint32_t b) {
+  return (b & 0x7FFFFFFFu) > kMaxAbsWeightBits;
+}
+
 // ------------------------------------------------------------- order key ----
 // Total order of (score, logical index): score descending with NaN below every
 // number and +0 above -0, then index ascending.  The 32-bit score key is

@@ -45,7 +45,14 @@ enum : uint32_t {
   kErrCuda = 6,
   kErrInternal = 7,
   kErrTimeout = 8,
+  kErrInvalidValue = 10,
 };
+
+// Accepted value domain (the header's IDX_MAX_SCALE_BYTE / IDX_MAX_ABS_WEIGHT):
+// UE8M0 bytes <= 167 and finite weights of magnitude <= 2^24 keep every logit
+// below 2^93 and every score finite.
+constexpr uint32_t kMaxScaleByte = 167;
+constexpr uint32_t kMaxAbsWeightBits = 0x4B800000u;  // 2^24 as fp32
 
 struct BlockInfo {
   int32_t row0;       // first row

@@ -129,46 +129,82 @@ __device__ void mbar_drain(uint32_t bar, uint32_t parity) {
 
 // score = sum over heads of w * max(logit, 0) in fp32.
 //
-// Each head pair is rectified with two max-with-zero operations and folded into
-// one of four packed (f32x2) accumulators by a single paired FMA; four
-// accumulators keep the dependency chains short.  The fused and the dense
+// Each head pair is folded into one of four packed (f32x2) accumulators by a
+// single paired FMA; four accumulators keep the dependency chains short.  The
+// rectification is split between two pipes: accumulators 0 and 1 take
+// max(x, 0) (ALU pipe), accumulators 2 and 3 take |x| + x = 2 max(x, 0) (an
+// add with an absolute-value operand, FMA pipe) and so hold doubled sums,
+// which the final sum halves.  Both forms are exact for every logit of the
+// accepted value domain (|x| < 2^93), and scaling by 2 commutes with fp32
+// rounding away from the subnormal range, so the score equals the plain
+// sum_h w * max(x, 0) with the same association.  The fused and the dense
 // paths share this code, so their scores are bit-identical.
 
-// One head pair: acc += (relu(x0), relu(x1)) * (w0, w1), packed.  Written in
-// PTX so that the pair is formed in place from the TMEM-load registers.
-__device__ __forceinline__ void pair_fmnmx(uint64_t& acc, uint32_t x0, uint32_t x1, uint64_t w) {
-  asm("{\n\t.reg .f32 a, b;\n\t.reg .b64 v;\n\t"
-      "max.f32 a, %1, 0f00000000;\n\t"
-      "max.f32 b, %2, 0f00000000;\n\t"
-      "mov.b64 v, {a, b};\n\t"
-      "fma.rn.f32x2 %0, v, %3, %0;\n\t}"
-      : "+l"(acc)
-      : "f"(__uint_as_float(x0)), "f"(__uint_as_float(x1)), "l"(w));
+// One head pair: acc += (relu(x0), relu(x1)) * (w0, w1), packed (first
+// product: acc = ...).  Written in PTX so that the pair is formed in place
+// from the TMEM-load registers.
+template <bool kInit>
+__device__ __forceinline__ void pair_max(uint64_t& acc, uint32_t x0, uint32_t x1, uint64_t w) {
+  if (kInit)
+    asm("{\n\t.reg .f32 a, b;\n\t.reg .b64 v;\n\t"
+        "max.f32 a, %1, 0f00000000;\n\t"
+        "max.f32 b, %2, 0f00000000;\n\t"
+        "mov.b64 v, {a, b};\n\t"
+        "mul.rn.f32x2 %0, v, %3;\n\t}"
+        : "=l"(acc)
+        : "f"(__uint_as_float(x0)), "f"(__uint_as_float(x1)), "l"(w));
+  else
+    asm("{\n\t.reg .f32 a, b;\n\t.reg .b64 v;\n\t"
+        "max.f32 a, %1, 0f00000000;\n\t"
+        "max.f32 b, %2, 0f00000000;\n\t"
+        "mov.b64 v, {a, b};\n\t"
+        "fma.rn.f32x2 %0, v, %3, %0;\n\t}"
+        : "+l"(acc)
+        : "f"(__uint_as_float(x0)), "f"(__uint_as_float(x1)), "l"(w));
 }
 
-// The first product of each accumulator: acc = (relu(x0), relu(x1)) * (w0, w1).
-__device__ __forceinline__ void pair_fmnmx_init(uint64_t& acc, uint32_t x0, uint32_t x1, uint64_t w) {
-  asm("{\n\t.reg .f32 a, b;\n\t.reg .b64 v;\n\t"
-      "max.f32 a, %1, 0f00000000;\n\t"
-      "max.f32 b, %2, 0f00000000;\n\t"
-      "mov.b64 v, {a, b};\n\t"
-      "mul.rn.f32x2 %0, v, %3;\n\t}"
-      : "=l"(acc)
-      : "f"(__uint_as_float(x0)), "f"(__uint_as_float(x1)), "l"(w));
+// One head pair into a doubled accumulator: acc += (|x0| + x0, |x1| + x1) * (w0, w1).
+template <bool kInit>
+__device__ __forceinline__ void pair_abs(uint64_t& acc, uint32_t x0, uint32_t x1, uint64_t w) {
+  if (kInit)
+    asm("{\n\t.reg .f32 a, b, c, d;\n\t.reg .b64 v;\n\t"
+        "abs.f32 a, %1;\n\t"
+        "abs.f32 b, %2;\n\t"
+        "add.rn.f32 c, a, %1;\n\t"
+        "add.rn.f32 d, b, %2;\n\t"
+        "mov.b64 v, {c, d};\n\t"
+        "mul.rn.f32x2 %0, v, %3;\n\t}"
+        : "=l"(acc)
+        : "f"(__uint_as_float(x0)), "f"(__uint_as_float(x1)), "l"(w));
+  else
+    asm("{\n\t.reg .f32 a, b, c, d;\n\t.reg .b64 v;\n\t"
+        "abs.f32 a, %1;\n\t"
+        "abs.f32 b, %2;\n\t"
+        "add.rn.f32 c, a, %1;\n\t"
+        "add.rn.f32 d, b, %2;\n\t"
+        "mov.b64 v, {c, d};\n\t"
+        "fma.rn.f32x2 %0, v, %3, %0;\n\t}"
+        : "+l"(acc)
+        : "f"(__uint_as_float(x0)), "f"(__uint_as_float(x1)), "l"(w));
 }
 
-// Heads 2*P0 .. 2*P0+15 from one 16-column TMEM load.  P0 == 0 starts the four
-// accumulators with plain products instead of adding to zero: the sums differ
-// at most in the sign of an all-zero total, which head_sum_final normalises.
+// Heads 2*P0 .. 2*P0+15 from one 16-column TMEM load; head pair p goes to
+// accumulator p % 4.  P0 == 0 starts the four accumulators with plain
+// products instead of adding to zero: the sums differ at most in the sign of
+// an all-zero total, which head_sum_final normalises.
 template <int P0>
 __device__ __forceinline__ void head_sum_part(const uint32_t (&x)[16], const uint64_t (&w2)[32],
                                               uint64_t (&acc)[4]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {  // head pair (2p, 2p+1), p = P0 + i
-    if (P0 == 0 && i < 4)
-      pair_fmnmx_init(acc[i], x[2 * i], x[2 * i + 1], w2[i]);
-    else
-      pair_fmnmx(acc[i & 3], x[2 * i], x[2 * i + 1], w2[P0 + i]);
+    const bool init = P0 == 0 && i < 4;
+    if ((i & 3) < 2) {
+      if (init) pair_max<true>(acc[i & 3], x[2 * i], x[2 * i + 1], w2[P0 + i]);
+      else pair_max<false>(acc[i & 3], x[2 * i], x[2 * i + 1], w2[P0 + i]);
+    } else {
+      if (init) pair_abs<true>(acc[i & 3], x[2 * i], x[2 * i + 1], w2[P0 + i]);
+      else pair_abs<false>(acc[i & 3], x[2 * i], x[2 * i + 1], w2[P0 + i]);
+    }
   }
 }
 
@@ -182,10 +218,16 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
   return d;
 }
 
+__device__ __forceinline__ uint64_t half2(uint64_t a) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(0x3F0000003F000000ull));
+  return d;
+}
+
 // The four packed partial sums folded lane-wise ((acc0 + acc1) + (acc2 + acc3)),
-// then the two lanes added: three packed adds and one scalar add.
+// the doubled pair halved, then the two lanes added.
 __device__ __forceinline__ float head_sum_final(const uint64_t (&acc)[4]) {
-  const float2 t = unpack2(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])));
+  const float2 t = unpack2(add2(add2(acc[0], acc[1]), half2(add2(acc[2], acc[3]))));
   // + 0 turns an all-zero total of -0 into +0, the value a sum started at +0 has
   return (t.x + t.y) + 0.0f;
 }
@@ -455,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       uint32_t wnext[4] = {0u, 0u, 0u, 0u};
       bool have_next = false;
+      uint32_t sf_over = 0;  // K scale bytes of this unit's pages outside the domain
       for (int t = uv.u.t_begin; t < uv.u.t_end; ++t) {
         const uint32_t n = n_issued++;
         if ((n & 1u) != pw) continue;
@@ -480,6 +523,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           load_scales(pg0, pg1, wcur);
         }
+        sf_over |= scale_bytes_over(wcur[0]) | scale_bytes_over(wcur[1]) |
+                   scale_bytes_over(wcur[2]) | scale_bytes_over(wcur[3]);
         have_next = t + 2 < uv.u.t_end;
         if (have_next) {
           int32_t ng0, ng1;
@@ -512,6 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (__any_sync(0xffffffffu, sf_over != 0u) && lane == 0)
+        raise_status(hdr, kErrInvalidValue, 304);
     }
     if (lane == 0) {
       // wait for this warp's copies in flight (its stages have parity pw)
@@ -654,6 +701,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           };
           load_w2();
+          if (tg < kHeads) {
+            // the row's query scales (one word per head) and weights must lie
+            // in the accepted value domain
+            const uint32_t qsf = reinterpret_cast<const uint32_t*>(
+                smem + kOffSfbRaw + qb * kSfbAtomBytes + g * kRowSfBytes)[tg];
+            const uint32_t wb = reinterpret_cast<const uint32_t*>(
+                smem + kOffW + qb * kBlockWBytes + g * kHeads * 4)[tg];
+            if (scale_bytes_over(qsf) != 0u || weight_out_of_domain(wb))
+              raise_status(hdr, kErrInvalidValue, 323);
+          }
           uint32_t thi = 0, tlo = 0;  // threshold key (score key, ~index)
           uint32_t wcnt = 0;          // keys in this warp's append region
           uint64_t* wreg = cand + (uint32_t)qd * warp_region(TOPK);

@@ -73,9 +73,31 @@ typedef enum {
                                    candidates, or a plan bound was exceeded */
   IDX_ERR_TIMEOUT = 8,          /* a bounded device-side wait expired (the kernel returned
                                    instead of hanging) */
-  IDX_ERR_SCRATCH_LIMIT = 9     /* idx_topk_fp4_prefill_noalloc only: the call needs more
+  IDX_ERR_SCRATCH_LIMIT = 9,    /* idx_topk_fp4_prefill_noalloc only: the call needs more
                                    scratch than IDX_NOALLOC_SCRATCH_BYTES */
+  IDX_ERR_INVALID_VALUE = 10    /* an input value outside the accepted domain (see
+                                   IDX_MAX_SCALE_BYTE and IDX_MAX_ABS_WEIGHT): a scale byte
+                                   above 167 in the query block of a scored row or in a K page
+                                   that a window covers, or a weight of a scored row that is not
+                                   finite or exceeds 2^24 in magnitude */
 } idx_status_t;
+
+/*
+ * Accepted value domain (aiter#5309 Implementation: the operator fails closed
+ * rather than produce nonfinite scores).  Every UE8M0 scale byte the scorer
+ * reads -- the query block of each row it scores, and every K page under a
+ * scored window -- must be at most IDX_MAX_SCALE_BYTE (scale exponent at most
+ * +40; the NaN byte 255 is above it), and every weight of a scored row must be
+ * finite with magnitude at most IDX_MAX_ABS_WEIGHT.  A per-head logit is then
+ * below 2^93 in magnitude (at most 4 blocks x 32 products of E2M1 magnitudes
+ * <= 6, i.e. < 2^13, times 2^(40+40)) and a score below 64 * 2^24 * 2^93 =
+ * 2^123, so every score is finite.  A call that reads a value outside the
+ * domain returns IDX_ERR_INVALID_VALUE with -1 outputs.  Bytes the scorer never
+ * reads (pages outside every window, query blocks and weights of rows of
+ * length <= topk) are not checked.
+ */
+#define IDX_MAX_SCALE_BYTE 167
+#define IDX_MAX_ABS_WEIGHT 16777216.0f
 
 typedef enum { IDX_U8 = 1, IDX_I32 = 2, IDX_F32 = 3 } idx_dtype_t;
 
@@ -107,7 +129,8 @@ typedef struct {
  *   out_raw_idx   i32 [R, topk]    logical C4 position or -1; may be NULL
  *
  * Rows whose window is longer than topk are ordered by (score desc, position asc).
- * Scale bytes of 255 (NaN) are outside the contract.  The operation is the one
+ * Scale bytes and weights must lie in the accepted domain above (else
+ * IDX_ERR_INVALID_VALUE).  The operation is the one
  * defined at the top of this file (aiter#5309 Summary and Implementation;
  * aiter#5282 Changes and Scope).
  */

@@ -160,3 +160,35 @@ def compare_rows(p, rows, g_raw, g_phys, o_raw, o_phys, o_scores_by_row):
             assert abs(v - kth) <= ATOL + RTOL * abs(kth) + 1e-7 * abs(kth), (r, idx, v, kth)
         n_diff += len(diff) // 2
     return n_diff
+
+
+def sample_rows(p, total=32, seed=0):
+    """First and last row of every request, random rows (at least `total` over
+    all requests, spread evenly), and the first short rows."""
+    rng = np.random.default_rng(seed)
+    rows = set()
+    reqs = np.unique(p.row_req)
+    per_req = max(2, -(-total // len(reqs)))
+    for req in reqs:
+        idx = np.nonzero(p.row_req == req)[0]
+        rows.update([int(idx[0]), int(idx[-1])])
+        rows.update(int(x) for x in rng.choice(idx, size=min(per_req, idx.size), replace=False))
+    short = np.nonzero(p.lengths() <= p.topk)[0]
+    rows.update(int(x) for x in short[:4])
+    return np.array(sorted(rows), dtype=np.int32)
+
+
+def check_against_oracle(p, g_phys, g_raw, rows=None, max_diff=None):
+    """Compare the GPU outputs of `rows` (default: every row; g_phys/g_raw hold
+    all rows) with the oracle by the rules of compare_rows; returns the number
+    of boundary differences."""
+    import oracle
+    if rows is None:
+        rows = np.arange(p.rows, dtype=np.int32)
+    rows = np.asarray(rows, dtype=np.int32)
+    o_phys, o_raw, _, inexact = oracle.prefill_rows(p, rows=rows, with_kth=True)
+    assert inexact == 0
+    scores = {int(r): oracle.row_scores(p, int(r))[0] for r in rows if p.lengths()[r] > p.topk}
+    n = compare_rows(p, rows, g_raw[rows], g_phys[rows], o_raw, o_phys, scores)
+    assert n <= (max_diff if max_diff is not None else max(2, len(rows) // 4)), n
+    return n

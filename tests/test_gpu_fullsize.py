@@ -24,22 +24,6 @@ from tests import helpers as H
 pytestmark = pytest.mark.gpu
 
 
-def sample_rows(p, total=32, seed=0):
-    """First and last row of every request, random rows (at least `total` over
-    all requests, spread evenly), and the first short rows."""
-    rng = np.random.default_rng(seed)
-    rows = set()
-    reqs = np.unique(p.row_req)
-    per_req = max(2, -(-total // len(reqs)))
-    for req in reqs:
-        idx = np.nonzero(p.row_req == req)[0]
-        rows.update([int(idx[0]), int(idx[-1])])
-        rows.update(int(x) for x in rng.choice(idx, size=min(per_req, idx.size), replace=False))
-    short = np.nonzero(p.lengths() <= p.topk)[0]
-    rows.update(int(x) for x in short[:4])
-    return np.array(sorted(rows), dtype=np.int32)
-
-
 def composite_keys(sc_rows, base_idx):
     """int64 order key: score key (NaN lowest, +0 above -0) << 31 | (2^31-1-index)."""
     import torch
@@ -116,7 +100,7 @@ def check_workload(p):
     d = H.to_device(p)
     code, g_phys, g_raw = H.run_fused(p, d)
     assert code == 0
-    rows = sample_rows(p)
+    rows = H.sample_rows(p)
     o_phys, o_raw, kth, inexact = oracle.prefill_rows(p, rows=rows, with_kth=True)
     assert inexact == 0
     scores = {int(r): oracle.row_scores(p, int(r))[0] for r in rows

@@ -1,7 +1,8 @@
 """The page-interleaved K cache entry point: each physical page's codes
-followed by its scales in one 4352-byte record.  Built from the same data as
-the two-tensor layout, it must give identical outputs; the record width is
-checked on the host."""
+followed by its scales in one 4352-byte record.  Its outputs are compared with
+the oracle (every row of the small cases, sampled rows of the 1024-row
+workloads) and, built from the same data as the two-tensor layout, must equal
+that layout's outputs; the record width is checked on the host."""
 import numpy as np
 import pytest
 
@@ -32,16 +33,19 @@ def _paged_call(p, d, k_pages, K=None, raise_on_error=True):
     return code, phys.cpu().numpy(), raw.cpu().numpy()
 
 
-@pytest.mark.parametrize("which", ["small512", "small1024", "config1"])
-def test_paged_equals_two_tensor_layout(which):
+@pytest.mark.parametrize("which", ["small512", "small1024", "config1", "config4"])
+def test_paged_matches_oracle_and_two_tensor_layout(which):
     import torch
     p = {"small512": lambda: inputs.small_problem(seed=21, topk=512),
          "small1024": lambda: inputs.small_problem(seed=22, topk=1024),
-         "config1": lambda: inputs.config(1)}[which]()
+         "config1": lambda: inputs.config(1),
+         "config4": lambda: inputs.config(4)}[which]()
     d = H.to_device(p)
     kp = torch.from_numpy(_interleave(p)).cuda()
     code, phys, raw = _paged_call(p, d, kp)
     assert code == 0
+    rows = None if p.rows <= 64 else H.sample_rows(p, total=12, seed=5)
+    H.check_against_oracle(p, phys, raw, rows)
     code2, want_phys, want_raw = H.run_fused(p, d)
     assert code2 == 0
     np.testing.assert_array_equal(raw, want_raw)

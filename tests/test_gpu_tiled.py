@@ -1,7 +1,8 @@
-"""The context-tiled comparison path gives the fused path's outputs (same
-scoring arithmetic, same order keys), for several chunk widths including ones
-that split pages' worth of positions across chunks and chunks no row reaches;
-bad chunk widths are refused."""
+"""The context-tiled comparison path against the oracle (every row of the small
+cases, sampled rows of the 1024-row workloads) and against the fused path
+(identical outputs: same scoring arithmetic, same order keys), for several
+chunk widths including ones that split pages' worth of positions across chunks
+and chunks no row reaches; bad chunk widths are refused."""
 import numpy as np
 import pytest
 
@@ -24,7 +25,7 @@ def _tiled(p, d, tile, raise_on_error=True):
 
 @pytest.mark.parametrize("which,tile", [("small512", 1024), ("small1024", 1152),
                                         ("config1", 4096), ("config1", 65536), ("config4", 16384)])
-def test_tiled_equals_fused(which, tile):
+def test_tiled_matches_oracle_and_fused(which, tile):
     p = {"small512": lambda: inputs.small_problem(seed=31, topk=512),
          "small1024": lambda: inputs.small_problem(seed=32, topk=1024),
          "config1": lambda: inputs.config(1),
@@ -32,6 +33,8 @@ def test_tiled_equals_fused(which, tile):
     d = H.to_device(p)
     code, phys, raw = _tiled(p, d, tile)
     assert code == 0
+    rows = None if p.rows <= 64 else H.sample_rows(p, total=12, seed=tile)
+    H.check_against_oracle(p, phys, raw, rows)
     code2, want_phys, want_raw = H.run_fused(p, d)
     assert code2 == 0
     np.testing.assert_array_equal(raw, want_raw)
