@@ -22,6 +22,7 @@ from . import _lib
 __all__ = ["IdxError", "SUPPORTED_K", "idx_topk_fp4_prefill", "idx_topk_fp4_prefill_noalloc",
            "idx_topk_fp4_prefill_host",
            "idx_topk_fp4_prefill_async", "idx_topk_fp4_prefill_paged",
+           "idx_topk_fp4_prefill_shard", "idx_topk_merge_shards",
            "idx_dense_topk_fp4_prefill", "idx_tiled_topk_fp4_prefill",
            "idx_fp4_debug_scores", "idx_topk_select_scores", "idx_topk_supported_k",
            "idx_topk_status_string", "idx_topk_fp4_scratch_bytes", "idx_topk_scratch_high_water",
@@ -145,6 +146,34 @@ def idx_topk_fp4_prefill_noalloc(q_fp4, q_scale, k_cache_fp4, k_scale, weights, 
     code = lib.idx_topk_fp4_prefill_noalloc(*[_ref(d) for d in ds[:9]], int(topk), _ref(ds[9]),
                                             _ref(ds[10]), _stream(stream))
     return _check(code, "idx_topk_fp4_prefill_noalloc", raise_on_error)
+
+
+def idx_topk_fp4_prefill_shard(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table,
+                               row_req, row_start, row_end, ctx_begin, ctx_end, topk, out_score,
+                               out_raw_idx, stream=None, raise_on_error=True) -> int:
+    """One context shard: each row longer than topk scored against the part of
+    its window inside [ctx_begin, ctx_end); writes that part's exact TopK
+    (scores f32 and positions i32 [R, topk], -1 / NaN padded) in place."""
+    lib = _lib.load()
+    ds = [_desc(t) for t in (q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                             row_start, row_end, out_score, out_raw_idx)]
+    code = lib.idx_topk_fp4_prefill_shard(*[_ref(d) for d in ds[:9]], int(ctx_begin),
+                                          int(ctx_end), int(topk), _ref(ds[9]), _ref(ds[10]),
+                                          _stream(stream))
+    return _check(code, "idx_topk_fp4_prefill_shard", raise_on_error)
+
+
+def idx_topk_merge_shards(shard_score, shard_raw, page_table, row_req, row_start, row_end, topk,
+                          out_phys_slot, out_raw_idx=None, stream=None,
+                          raise_on_error=True) -> int:
+    """Exact merge of S context-shard lists [S, R, topk] into the TopK outputs
+    (short-row contract and page mapping included)."""
+    lib = _lib.load()
+    ds = [_desc(t) for t in (shard_score, shard_raw, page_table, row_req, row_start, row_end,
+                             out_phys_slot, out_raw_idx)]
+    code = lib.idx_topk_merge_shards(*[_ref(d) for d in ds[:6]], int(topk), _ref(ds[6]),
+                                     _ref(ds[7]), _stream(stream))
+    return _check(code, "idx_topk_merge_shards", raise_on_error)
 
 
 def idx_dense_topk_fp4_prefill(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,

@@ -93,6 +93,13 @@ EXPORTS = {
     "idx_topk_fp4_prefill_noalloc": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
                                      [ctypes.c_int32, ctypes.POINTER(IdxTensor),
                                       ctypes.POINTER(IdxTensor), ctypes.c_void_p]),
+    "idx_topk_fp4_prefill_shard": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
+                                   [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                    ctypes.POINTER(IdxTensor), ctypes.POINTER(IdxTensor),
+                                    ctypes.c_void_p]),
+    "idx_topk_merge_shards": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 6 +
+                              [ctypes.c_int32, ctypes.POINTER(IdxTensor),
+                               ctypes.POINTER(IdxTensor), ctypes.c_void_p]),
     "idx_tiled_topk_fp4_prefill": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
                                    [ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(IdxTensor),
                                     ctypes.POINTER(IdxTensor), ctypes.c_void_p]),

@@ -56,9 +56,13 @@ __device__ __forceinline__ void sort_in_thread(uint64_t (&v)[E], int g0, int siz
 // stay in the thread, distances below 32*E go between the lanes of a warp,
 // and only the larger ones pass through shared memory.  The caller has filled
 // buf[0, TOPK) (zero keys pad an underfilled row) before a barrier.
-template <int TOPK>
+// SCORES: also write the keys' scores to out_score; DUP: raise on dup_hdr when
+// two emitted keys are equal (a position listed twice by the shard merge).
+template <int TOPK, bool SCORES = false, bool DUP = false>
 __device__ __forceinline__ void sort_emit(uint64_t* buf, int tid, const int32_t* row_pt,
-                                          int32_t* out_raw, int32_t* out_phys) {
+                                          int32_t* out_raw, int32_t* out_phys,
+                                          float* out_score = nullptr,
+                                          PlanHeader* dup_hdr = nullptr) {
   constexpr int E = TOPK / kFinThreads;
   static_assert(E == 2 || E == 4, "keys per thread");
   const int g0 = tid * E;
@@ -100,11 +104,27 @@ __device__ __forceinline__ void sort_emit(uint64_t* buf, int tid, const int32_t*
       }
     }
   }
+  if (DUP) {
+    // the merge of context-shard lists: a position reported twice would show
+    // up as two equal (nonzero) neighbours of the sorted keys
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < E; ++e) buf[g0 + e] = v[e];
+    __syncthreads();
+    bool dup = false;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int i = g0 + e;
+      dup |= i + 1 < TOPK && v[e] != 0ull && buf[i + 1] == v[e];
+    }
+    if (dup) raise_status(dup_hdr, kErrInvalidMetadata, 422);
+  }
   int32_t raw[E], phys[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     raw[e] = v[e] != 0ull ? key_index(v[e]) : -1;
     phys[e] = map_phys(row_pt, raw[e]);
+    if (SCORES) out_score[g0 + e] = key_score(v[e]);
   }
   // E consecutive outputs per thread; rows start at multiples of 2 KB of a
   // 16-byte aligned base
@@ -195,8 +215,9 @@ struct TeamSmem {
   uint32_t team_ok[kTeams];
 };
 
-// The rows of CTA `blk` of the team grid (kTeams rows per CTA).
-template <int TOPK>
+// The rows of CTA `blk` of the team grid (kTeams rows per CTA).  SCORES: a
+// context shard's emission (p.out_score set), see FinishParams.
+template <int TOPK, bool SCORES>
 __device__ __forceinline__ void team_rows(const FinishParams& p, int64_t blk, TeamSmem<TOPK>& ts) {
   constexpr int W = TeamSmem<TOPK>::W;
   constexpr int kTeams = TeamSmem<TOPK>::kTeams;
@@ -219,12 +240,15 @@ __device__ __forceinline__ void team_rows(const FinishParams& p, int64_t blk, Te
       p.page_table ? p.page_table + (int64_t)p.row_req[r] * p.max_pages : nullptr;
   int32_t* out_raw = p.out_raw ? p.out_raw + r * TOPK : nullptr;
   int32_t* out_phys = p.out_phys ? p.out_phys + r * TOPK : nullptr;
+  float* out_score = SCORES ? p.out_score + r * TOPK : nullptr;
   const int t = tw * 32 + lane;  // thread within the team
-  if (len <= TOPK) {
+  // a context shard scores every nonempty clipped window, however short
+  if (len <= (SCORES ? 0 : TOPK)) {
     for (int i = t; i < TOPK; i += 32 * W) {
       const int32_t raw = i < len ? s0 + i : -1;
       if (out_raw) out_raw[i] = raw;
       if (out_phys) out_phys[i] = map_phys(row_pt, raw);
+      if (SCORES) out_score[i] = __uint_as_float(0x7FC00000u);
     }
     return;
   }
@@ -258,6 +282,9 @@ __device__ __forceinline__ void team_rows(const FinishParams& p, int64_t blk, Te
       *reinterpret_cast<int4*>(out_raw + g0 + e) = make_int4(raw[0], raw[1], raw[2], raw[3]);
     if (out_phys)
       *reinterpret_cast<int4*>(out_phys + g0 + e) = make_int4(phys[0], phys[1], phys[2], phys[3]);
+    if (SCORES)
+      *reinterpret_cast<float4*>(out_score + g0 + e) =
+          make_float4(key_score(v[e]), key_score(v[e + 1]), key_score(v[e + 2]), key_score(v[e + 3]));
   }
 }
 
@@ -273,9 +300,14 @@ struct FinSmem {
   uint64_t tau;
 };
 
+// Where finish_row takes a row's candidates from.
+enum FinSrc : int { kSrcUnits = 0, kSrcDense = 1, kSrcShards = 2 };
+
 // One row, by the whole CTA (every early return is uniform over the CTA).
-template <int TOPK, bool DENSE>
+// SCORES: a context shard's emission (p.out_score set), see FinishParams.
+template <int TOPK, int SRC, bool SCORES>
 __device__ __forceinline__ void finish_row(const FinishParams& p, int64_t r, FinSmem& sm) {
+  constexpr bool DENSE = SRC != kSrcUnits;  // the closed form of short rows is ours
   uint64_t* buf = sm.buf;
   uint32_t* hist = sm.hist;
   uint32_t* bc = sm.bc;
@@ -288,8 +320,9 @@ __device__ __forceinline__ void finish_row(const FinishParams& p, int64_t r, Fin
       p.page_table ? p.page_table + (int64_t)p.row_req[r] * p.max_pages : nullptr;
   int32_t* out_raw = p.out_raw ? p.out_raw + (int64_t)r * TOPK : nullptr;
   int32_t* out_phys = p.out_phys ? p.out_phys + (int64_t)r * TOPK : nullptr;
+  float* out_score = SCORES ? p.out_score + (int64_t)r * TOPK : nullptr;
 
-  if (len <= TOPK) {
+  if (len <= (SCORES ? 0 : TOPK)) {
     if constexpr (DENSE) {
       for (int i = tid; i < TOPK; i += kFinThreads) {
         const int32_t raw = i < len ? s0 + i : -1;
@@ -309,7 +342,32 @@ __device__ __forceinline__ void finish_row(const FinishParams& p, int64_t r, Fin
   }
   __syncthreads();
   uint64_t t = 0;
-  if constexpr (DENSE) {
+  if constexpr (SRC == kSrcShards) {
+    // the union of the row's context-shard lists; every listed position must
+    // lie in the row's window
+    bool bad = false;
+    for (int k = 0; k < p.n_shards; ++k) {
+      const int64_t off = ((int64_t)k * p.rows + r) * TOPK;
+      for (int base = 0; base < TOPK; base += kFinBatch) {
+        bool over = false;
+#pragma unroll
+        for (int e = 0; e < kFinPer; ++e) {
+          const int i = base + e * kFinThreads + tid;
+          const int32_t raw = i < TOPK ? p.shard_raw[off + i] : -1;
+          const bool in = raw >= 0;
+          bad |= raw < -1 || (in && (raw < s0 || raw >= s1));
+          const uint64_t key = in ? order_key(p.shard_score[off + i], raw) : 0ull;
+          over |= sel_append(buf, &cnt, kFinCap, kFinCap - kFinBatch, in && key >= t, key);
+        }
+        if (bar_red_or(kFinBar, kFinThreads, over)) {
+          sel_compact<kFinThreads, kFinCap>(buf, &cnt, &tau, hist, bc, TOPK, tid, kFinBar, p.hdr,
+                                            nullptr, 0, 0, kErrInvalidMetadata);
+          t = *(volatile uint64_t*)&tau;
+        }
+      }
+    }
+    if (bad) raise_status(p.hdr, kErrInvalidMetadata, 420);
+  } else if constexpr (DENSE) {
     const float* src = p.scores + (int64_t)r * p.score_stride;
     for (int64_t base = s0; base < s1; base += kFinBatch) {
       bool over = false;
@@ -392,36 +450,41 @@ __device__ __forceinline__ void finish_row(const FinishParams& p, int64_t r, Fin
     }
   }
   __syncthreads();
-  sel_compact<kFinThreads, kFinCap>(buf, &cnt, &tau, hist, bc, TOPK, tid, kFinBar, p.hdr);
+  sel_compact<kFinThreads, kFinCap>(buf, &cnt, &tau, hist, bc, TOPK, tid, kFinBar, p.hdr, nullptr,
+                                    0, 0, SRC == kSrcShards ? kErrInvalidMetadata : kErrInternal);
   const uint32_t n = min(*(volatile uint32_t*)&cnt, (uint32_t)TOPK);
   if (n < (uint32_t)TOPK) {
-    // a window longer than topk must yield topk candidates
-    if (tid == 0) raise_status(p.hdr, kErrInternal, 400);
+    // a window of len positions yields min(len, topk) candidates (len > topk
+    // except for the clipped windows of a context shard)
+    if (tid == 0 && (!SCORES || n < (uint64_t)len))
+      raise_status(p.hdr, SRC == kSrcShards ? kErrInvalidMetadata : kErrInternal,
+                   SRC == kSrcShards ? 421 : 400);
     for (int i = n + tid; i < TOPK; i += kFinThreads) buf[i] = 0ull;
   }
   __syncthreads();
-  sort_emit<TOPK>(buf, tid, row_pt, out_raw, out_phys);
+  sort_emit<TOPK, SCORES, SRC == kSrcShards>(buf, tid, row_pt, out_raw, out_phys, out_score, p.hdr);
 }
 
 // Rows r = blk, blk + nblk, ...; the status is read once per row by one
 // thread so that the CTA's threads agree on it.
-template <int TOPK, bool DENSE>
+template <int TOPK, int SRC, bool SCORES>
 __device__ __forceinline__ void merge_rows(const FinishParams& p, int64_t blk, int64_t nblk,
                                            FinSmem& sm) {
   for (int64_t r = blk; r < p.rows; r += nblk) {
     if (threadIdx.x == 0) sm.ok = read_status(p.hdr) == kOk;
     __syncthreads();
     if (!sm.ok) return;
-    finish_row<TOPK, DENSE>(p, r, sm);
+    finish_row<TOPK, SRC, SCORES>(p, r, sm);
     __syncthreads();  // the row's shared state is free again
   }
 }
 
-// Exact TopK of the rows of a materialised score matrix (the dense path).
-template <int TOPK, bool DENSE>
+// Exact TopK of the rows of a materialised score matrix (the dense path), or
+// of the union of a row's context-shard lists.
+template <int TOPK, int SRC>
 __global__ void __launch_bounds__(kFinThreads) finish_kernel(FinishParams p) {
   __shared__ __align__(16) FinSmem sm;
-  merge_rows<TOPK, DENSE>(p, blockIdx.x, gridDim.x, sm);
+  merge_rows<TOPK, SRC, false>(p, blockIdx.x, gridDim.x, sm);
 }
 
 // The fused path's finishing step in one launch: CTAs [0, team_blocks) sort
@@ -433,36 +496,44 @@ union FinishShared {
   FinSmem merge;
 };
 
-template <int TOPK>
+template <int TOPK, bool SCORES>
 __global__ void __launch_bounds__(kFinThreads) finish_fused_kernel(FinishParams p, int team_blocks) {
   static_assert(kTeamThreads == kFinThreads, "one block shape for both paths");
   __shared__ __align__(16) FinishShared<TOPK> sh;
-  if ((int)blockIdx.x < team_blocks)
-    team_rows<TOPK>(p, blockIdx.x, sh.team);
-  else
-    merge_rows<TOPK, false>(p, (int64_t)blockIdx.x - team_blocks, (int64_t)gridDim.x - team_blocks,
-                            sh.merge);
-}
-
-// Row windows of a bare score matrix: 0 <= start <= end <= width.
-__global__ void validate_windows_kernel(const int32_t* row_start, const int32_t* row_end,
-                                        int32_t rows, int64_t width, PlanHeader* hdr) {
-  for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < rows;
-       r += (int64_t)gridDim.x * blockDim.x) {
-    const int32_t s = row_start[r], e = row_end[r];
-    if (s < 0 || e < s || (int64_t)e > width) raise_status(hdr, kErrInvalidMetadata, 410);
+  if ((int)blockIdx.x < team_blocks) {
+    team_rows<TOPK, SCORES>(p, blockIdx.x, sh.team);
+  } else {
+    merge_rows<TOPK, kSrcUnits, SCORES>(p, (int64_t)blockIdx.x - team_blocks,
+                                        (int64_t)gridDim.x - team_blocks, sh.merge);
   }
 }
 
-template <int TOPK, bool DENSE>
+// Row windows: 0 <= start <= end <= width, and (row_req non-null) a request
+// in [0, num_req).
+__global__ void validate_windows_kernel(const int32_t* row_start, const int32_t* row_end,
+                                        int32_t rows, int64_t width, const int32_t* row_req,
+                                        int32_t num_req, PlanHeader* hdr) {
+  for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < rows;
+       r += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t s = row_start[r], e = row_end[r];
+    bool bad = s < 0 || e < s || (int64_t)e > width;
+    if (row_req) bad |= row_req[r] < 0 || row_req[r] >= num_req;
+    if (bad) raise_status(hdr, kErrInvalidMetadata, 410);
+  }
+}
+
+template <int TOPK, int SRC>
 cudaError_t launch_t(const FinishParams& p, cudaStream_t stream) {
   const int merge_grid = p.rows < kFinGridCap ? p.rows : kFinGridCap;
-  if (DENSE) {
-    finish_kernel<TOPK, DENSE><<<merge_grid, kFinThreads, 0, stream>>>(p);
+  if (SRC != kSrcUnits) {
+    finish_kernel<TOPK, SRC><<<merge_grid, kFinThreads, 0, stream>>>(p);
   } else {
     constexpr int kTeams = TeamSmem<TOPK>::kTeams;
     const int team_grid = (p.rows + kTeams - 1) / kTeams;
-    finish_fused_kernel<TOPK><<<team_grid + merge_grid, kFinThreads, 0, stream>>>(p, team_grid);
+    if (p.out_score)
+      finish_fused_kernel<TOPK, true><<<team_grid + merge_grid, kFinThreads, 0, stream>>>(p, team_grid);
+    else
+      finish_fused_kernel<TOPK, false><<<team_grid + merge_grid, kFinThreads, 0, stream>>>(p, team_grid);
   }
   return cudaGetLastError();
 }
@@ -471,10 +542,16 @@ cudaError_t launch_t(const FinishParams& p, cudaStream_t stream) {
 
 cudaError_t launch_finish(const FinishParams& p, cudaStream_t stream) {
   if (p.rows <= 0) return cudaSuccess;
-  const bool dense = p.scores != nullptr;
-  if (p.topk == 512) return dense ? launch_t<512, true>(p, stream) : launch_t<512, false>(p, stream);
-  if (p.topk == 1024)
-    return dense ? launch_t<1024, true>(p, stream) : launch_t<1024, false>(p, stream);
+  const int src = p.shard_raw ? kSrcShards : (p.scores ? kSrcDense : kSrcUnits);
+  if (p.topk == 512) {
+    if (src == kSrcShards) return launch_t<512, kSrcShards>(p, stream);
+    return src == kSrcDense ? launch_t<512, kSrcDense>(p, stream) : launch_t<512, kSrcUnits>(p, stream);
+  }
+  if (p.topk == 1024) {
+    if (src == kSrcShards) return launch_t<1024, kSrcShards>(p, stream);
+    return src == kSrcDense ? launch_t<1024, kSrcDense>(p, stream)
+                            : launch_t<1024, kSrcUnits>(p, stream);
+  }
   return cudaErrorInvalidValue;
 }
 
@@ -609,11 +686,13 @@ cudaError_t launch_publish_status(const PlanHeader* hdr, uint32_t* status_out, i
 }
 
 cudaError_t launch_validate_windows(const int32_t* row_start, const int32_t* row_end, int32_t rows,
-                                    int64_t width, PlanHeader* hdr, cudaStream_t stream) {
+                                    int64_t width, PlanHeader* hdr, cudaStream_t stream,
+                                    const int32_t* row_req, int32_t num_req) {
   if (rows <= 0) return cudaSuccess;
   int blocks = (rows + 255) / 256;
   if (blocks > 1024) blocks = 1024;
-  validate_windows_kernel<<<blocks, 256, 0, stream>>>(row_start, row_end, rows, width, hdr);
+  validate_windows_kernel<<<blocks, 256, 0, stream>>>(row_start, row_end, rows, width, row_req,
+                                                      num_req, hdr);
   return cudaGetLastError();
 }
 

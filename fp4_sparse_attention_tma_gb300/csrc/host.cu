@@ -911,6 +911,224 @@ int run_tiled(const Call& c, int32_t tile, cudaStream_t stream) {
   return IDX_OK;
 }
 
+// ------------------------------------------------ context-parallel pieces ----
+//
+// A context shard: every row is scored against the part of its window inside
+// [c0, c1) only, and emits that part's exact TopK with the scores (sorted,
+// padded with -1 / NaN).  Rows whose whole window is at most topk long emit
+// nothing: the merge gives them the closed form.  The shards of a context
+// partition, gathered into [S, rows, topk] lists, are merged exactly by
+// run_merge_shards ("[FlyDSL][DSv4] Prototype FP4 MQA streaming TopK",
+// ROCm/aiter#5282, Changes: exact merge of split candidates; "[AMD][DSv4] Add
+// experimental AITER FP4 streaming TopK", sglang#38101, Changes: context-
+// parallel paths).
+int run_shard(const Call& c, int32_t c0, int32_t c1, const idx_tensor_t* out_score,
+              cudaStream_t stream) {
+  const int64_t R0 = c.q_fp4 ? c.q_fp4->shape[0] : 0;
+  int st = check_output(c.out_raw, R0, c.topk);
+  if (st) return st;
+  if ((st = check_tensor(out_score, IDX_F32, 2))) return st;
+  if (out_score->shape[0] != R0 || out_score->shape[1] != c.topk) return IDX_ERR_INVALID_ARGUMENT;
+  Outputs outs;
+  outs.t[0] = c.out_raw;
+  outs.t[1] = out_score;  // 0xFF bytes: NaN scores
+  const idx_tensor_t* all[] = {c.q_fp4, c.q_scale, c.k_cache_fp4, c.k_scale, c.weights,
+                               c.page_table, c.row_req, c.row_start, c.row_end, c.out_raw,
+                               out_score};
+  int dev = -1;
+  if ((st = common_device(all, 11, &dev))) return st;
+  DeviceGuard guard(dev);
+  if (!guard.ok()) return IDX_ERR_CUDA;
+  st = check_stream(stream, dev);
+  if (st == IDX_ERR_UNSUPPORTED) return st;
+  auto fail = [&](int code) {
+    fill_minus_one(outs, stream);
+    return code;
+  };
+  if (st) return fail(st);
+  if (!topk_supported(c.topk)) return fail(IDX_ERR_UNSUPPORTED);
+  if (c0 < 0 || c1 < c0) return fail(IDX_ERR_INVALID_ARGUMENT);
+  Sizes sz;
+  if ((st = check_inputs(c.q_fp4, c.q_scale, c.k_cache_fp4, c.k_scale, c.weights, c.page_table,
+                         c.row_req, c.row_start, c.row_end, &sz)))
+    return fail(st);
+  if (sz.rows == 0) return IDX_OK;
+  DeviceState* ds = nullptr;
+  if ((st = device_state(dev, &ds))) return fail(st);
+  if (!(ds->cc_major == 10 && ds->cc_minor == 3)) return fail(IDX_ERR_UNSUPPORTED);
+  const int grid = ds->sm_count;
+  const int64_t R = sz.rows;
+  Scratch s;
+  s.L = scratch_layout(R, c.topk, grid, true);
+  const size_t off_win = align_up(s.L.total, 256);
+  const size_t total = off_win + align_up((size_t)R * 8, 256);
+  if (cudaMallocFromPoolAsync(&s.base, total, ds->pool, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(IDX_ERR_CUDA);
+  }
+  cudaMemsetAsync(s.hdr(), 0, sizeof(PlanHeader), stream);
+  int32_t* cs = s.at<int32_t>(off_win);
+  int32_t* ce = cs + R;
+  int cuda_err = 0;
+  // the whole windows first (the clipped ones are what the plan checks)
+  cuda_err |= launch_validate_windows((const int32_t*)c.row_start->data,
+                                      (const int32_t*)c.row_end->data, (int32_t)R,
+                                      sz.max_pages * kPage, s.hdr(), stream,
+                                      (const int32_t*)c.row_req->data, (int32_t)sz.num_req) !=
+              cudaSuccess;
+  cuda_err |= launch_clip_windows((const int32_t*)c.row_start->data,
+                                  (const int32_t*)c.row_end->data, (int32_t)R, c0, c1, c.topk, cs,
+                                  ce, stream) != cudaSuccess;
+  PlanParams pp{};
+  pp.row_req = (const int32_t*)c.row_req->data;
+  pp.row_start = cs;
+  pp.row_end = ce;
+  pp.page_table = (const int32_t*)c.page_table->data;
+  pp.rows = (int32_t)R;
+  pp.num_req = (int32_t)sz.num_req;
+  pp.max_pages = (int32_t)sz.max_pages;
+  pp.num_pages = (int32_t)sz.num_pages;
+  pp.score_thr = 0;  // every nonempty clipped window is scored
+  pp.grid = grid;
+  pp.check_end_le = -1;
+  pp.max_units = s.L.max_units;
+  pp.max_row_slots = s.L.max_row_slots;
+  pp.hdr = s.hdr();
+  pp.row_block = s.at<int32_t>(s.L.row_block);
+  pp.blocks = s.at<BlockInfo>(s.L.blocks);
+  pp.units = s.at<UnitInfo>(s.L.units);
+  pp.sched = s.at<int32_t>(s.L.sched);
+  cuda_err |= launch_plan(pp, stream) != cudaSuccess;
+  CUtensorMap tmap_k, tmap_q;
+  const KSource ks = k_source(c);
+  if (encode_k_pages(&tmap_k, ks.codes, (uint64_t)sz.num_pages, ks.page_bytes) ||
+      encode_2d_u8(&tmap_q, c.q_fp4->data, (uint64_t)R * kHeads, kRowsPerChunk * kHeads)) {
+    uint32_t dummy;
+    read_status_and_free(s, stream, &dummy);
+    return fail(IDX_ERR_CUDA);
+  }
+  ScoreParams sp{};
+  sp.q_scale = (const uint8_t*)c.q_scale->data;
+  sp.k_scale = ks.scales;
+  sp.k_scale_stride = ks.scale_stride_words;
+  sp.weights = (const float*)c.weights->data;
+  sp.page_table = pp.page_table;
+  sp.row_start = cs;
+  sp.row_end = ce;
+  sp.rows = pp.rows;
+  sp.max_pages = pp.max_pages;
+  sp.num_pages = pp.num_pages;
+  sp.topk = c.topk;
+  sp.mode = kModeSelect;
+  sp.score_thr = 0;
+  sp.hdr = pp.hdr;
+  sp.blocks = pp.blocks;
+  sp.units = pp.units;
+  sp.sched = pp.sched;
+  sp.cand_cnt = s.at<uint32_t>(s.L.cand_cnt);
+  sp.cand_keys = s.at<uint64_t>(s.L.cand_keys);
+  cuda_err |= launch_score(tmap_k, tmap_q, sp, grid, stream) != cudaSuccess;
+  FinishParams fp{};
+  fp.row_req = pp.row_req;
+  fp.row_start = cs;
+  fp.row_end = ce;
+  fp.page_table = nullptr;  // a shard emits positions and scores, no slots
+  fp.rows = pp.rows;
+  fp.max_pages = pp.max_pages;
+  fp.topk = c.topk;
+  fp.hdr = pp.hdr;
+  fp.row_block = pp.row_block;
+  fp.blocks = pp.blocks;
+  fp.cand_cnt = sp.cand_cnt;
+  fp.cand_keys = sp.cand_keys;
+  fp.out_raw = (int32_t*)c.out_raw->data;
+  fp.out_score = (float*)out_score->data;
+  cuda_err |= launch_finish(fp, stream) != cudaSuccess;
+  uint32_t status = 0;
+  st = read_status_and_free(s, stream, &status);
+  if (cuda_err || st || cudaGetLastError() != cudaSuccess) return fail(IDX_ERR_CUDA);
+  if (status != kOk) return fail((int)status);
+  return IDX_OK;
+}
+
+int run_merge_shards(const idx_tensor_t* shard_score, const idx_tensor_t* shard_raw,
+                     const idx_tensor_t* page_table, const idx_tensor_t* row_req,
+                     const idx_tensor_t* row_start, const idx_tensor_t* row_end, int32_t topk,
+                     const idx_tensor_t* out_phys, const idx_tensor_t* out_raw,
+                     cudaStream_t stream) {
+  if (!out_phys) return IDX_ERR_INVALID_ARGUMENT;
+  const int64_t R = out_phys->shape[0];
+  int st = check_output(out_phys, R, topk);
+  if (st) return st;
+  if (out_raw && (st = check_output(out_raw, R, topk))) return st;
+  Outputs outs;
+  outs.t[0] = out_phys;
+  outs.t[1] = out_raw;
+  const idx_tensor_t* all[] = {shard_score, shard_raw, page_table, row_req, row_start, row_end,
+                               out_phys, out_raw};
+  int dev = -1;
+  if ((st = common_device(all, 8, &dev))) return st;
+  DeviceGuard guard(dev);
+  if (!guard.ok()) return IDX_ERR_CUDA;
+  st = check_stream(stream, dev);
+  if (st == IDX_ERR_UNSUPPORTED) return st;
+  auto fail = [&](int code) {
+    fill_minus_one(outs, stream);
+    return code;
+  };
+  if (st) return fail(st);
+  if (!topk_supported(topk)) return fail(IDX_ERR_UNSUPPORTED);
+  if ((st = check_tensor(shard_score, IDX_F32, 3)) || (st = check_tensor(shard_raw, IDX_I32, 3)) ||
+      (st = check_tensor(page_table, IDX_I32, 2)) || (st = check_tensor(row_req, IDX_I32, 1)) ||
+      (st = check_tensor(row_start, IDX_I32, 1)) || (st = check_tensor(row_end, IDX_I32, 1)))
+    return fail(st);
+  const int64_t S = shard_raw->shape[0];
+  for (int i = 0; i < 3; ++i)
+    if (shard_score->shape[i] != shard_raw->shape[i]) return fail(IDX_ERR_INVALID_ARGUMENT);
+  if (S < 1 || shard_raw->shape[1] != R || shard_raw->shape[2] != topk ||
+      row_req->shape[0] != R || row_start->shape[0] != R || row_end->shape[0] != R)
+    return fail(IDX_ERR_INVALID_ARGUMENT);
+  const int64_t num_req = page_table->shape[0], max_pages = page_table->shape[1];
+  if (R > INT32_MAX || S > INT32_MAX || num_req > INT32_MAX || max_pages * (int64_t)kPage > INT32_MAX)
+    return fail(IDX_ERR_OVERFLOW);
+  if (R == 0) return IDX_OK;
+  if (num_req < 1 || max_pages < 1) return fail(IDX_ERR_INVALID_ARGUMENT);
+  DeviceState* ds = nullptr;
+  if ((st = device_state(dev, &ds))) return fail(st);
+  if (!(ds->cc_major == 10 && ds->cc_minor == 3)) return fail(IDX_ERR_UNSUPPORTED);
+  Scratch s;
+  s.L = scratch_layout(0, topk, 0, false);
+  if (cudaMallocFromPoolAsync(&s.base, s.L.total, ds->pool, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(IDX_ERR_CUDA);
+  }
+  cudaMemsetAsync(s.hdr(), 0, sizeof(PlanHeader), stream);
+  int cuda_err = 0;
+  cuda_err |= launch_validate_windows((const int32_t*)row_start->data, (const int32_t*)row_end->data,
+                                      (int32_t)R, max_pages * kPage, s.hdr(), stream,
+                                      (const int32_t*)row_req->data, (int32_t)num_req) != cudaSuccess;
+  FinishParams fp{};
+  fp.row_req = (const int32_t*)row_req->data;
+  fp.row_start = (const int32_t*)row_start->data;
+  fp.row_end = (const int32_t*)row_end->data;
+  fp.page_table = (const int32_t*)page_table->data;
+  fp.rows = (int32_t)R;
+  fp.max_pages = (int32_t)max_pages;
+  fp.topk = topk;
+  fp.hdr = s.hdr();
+  fp.n_shards = (int32_t)S;
+  fp.shard_score = (const float*)shard_score->data;
+  fp.shard_raw = (const int32_t*)shard_raw->data;
+  fp.out_phys = (int32_t*)out_phys->data;
+  fp.out_raw = out_raw ? (int32_t*)out_raw->data : nullptr;
+  cuda_err |= launch_finish(fp, stream) != cudaSuccess;
+  uint32_t status = 0;
+  st = read_status_and_free(s, stream, &status);
+  if (cuda_err || st || cudaGetLastError() != cudaSuccess) return fail(IDX_ERR_CUDA);
+  if (status != kOk) return fail((int)status);
+  return IDX_OK;
+}
+
 // ------------------------------------------------ stream-ordered call ----
 //
 // The fused path with a caller workspace and a device status word: no
@@ -1216,6 +1434,27 @@ int idx_topk_fp4_prefill_paged(const idx_tensor_t* q_fp4, const idx_tensor_t* q_
   Call c{q_fp4, q_scale, nullptr, nullptr, weights, page_table, row_req, row_start, row_end,
          topk, out_phys_slot, out_raw_idx, nullptr, nullptr, Path::kFused, k_pages};
   return run(c, (cudaStream_t)stream);
+}
+
+int idx_topk_fp4_prefill_shard(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                               const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
+                               const idx_tensor_t* weights, const idx_tensor_t* page_table,
+                               const idx_tensor_t* row_req, const idx_tensor_t* row_start,
+                               const idx_tensor_t* row_end, int32_t ctx_begin, int32_t ctx_end,
+                               int32_t topk, const idx_tensor_t* out_score,
+                               const idx_tensor_t* out_raw_idx, idx_stream_t stream) {
+  Call c{q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req, row_start, row_end,
+         topk, nullptr, out_raw_idx, nullptr, nullptr, Path::kFused};
+  return run_shard(c, ctx_begin, ctx_end, out_score, (cudaStream_t)stream);
+}
+
+int idx_topk_merge_shards(const idx_tensor_t* shard_score, const idx_tensor_t* shard_raw,
+                          const idx_tensor_t* page_table, const idx_tensor_t* row_req,
+                          const idx_tensor_t* row_start, const idx_tensor_t* row_end,
+                          int32_t topk, const idx_tensor_t* out_phys_slot,
+                          const idx_tensor_t* out_raw_idx, idx_stream_t stream) {
+  return run_merge_shards(shard_score, shard_raw, page_table, row_req, row_start, row_end, topk,
+                          out_phys_slot, out_raw_idx, (cudaStream_t)stream);
 }
 
 int idx_tiled_topk_fp4_prefill(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,

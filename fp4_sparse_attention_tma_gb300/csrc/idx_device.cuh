@@ -67,6 +67,14 @@ __device__ __forceinline__ int32_t key_index(uint64_t key) {
   return (int32_t)(~(uint32_t)(key & 0xffffffffu));
 }
 
+// The score of a key (the inverse of score_key on its high word); the empty
+// key 0 gives NaN.
+__device__ __forceinline__ float key_score(uint64_t key) {
+  const uint32_t k = (uint32_t)(key >> 32);
+  const uint32_t b = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+  return key == 0ull ? __uint_as_float(0x7FC00000u) : __uint_as_float(b);
+}
+
 // ------------------------------------------------------------- smem / PTX ----
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

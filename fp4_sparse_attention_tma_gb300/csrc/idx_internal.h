@@ -194,6 +194,15 @@ struct FinishParams {
   int64_t score_stride;
   int32_t* out_phys;          // [rows, topk] or null
   int32_t* out_raw;           // [rows, topk] or null
+  // context shard (out_score non-null): every nonempty (clipped) window was
+  // scored whatever its length; each row emits its sorted TopK positions with
+  // their scores, padded with -1 / NaN, and no physical slots
+  float* out_score;           // [rows, topk] or null
+  // merge of context-shard lists: n_shards lists of [rows, topk] (score, position)
+  int32_t n_shards;
+  int32_t pad2;
+  const float* shard_score;   // [n_shards, rows, topk]
+  const int32_t* shard_raw;   // [n_shards, rows, topk], -1 = empty entry
 };
 
 }  // namespace idxk

@@ -43,13 +43,16 @@ cudaError_t launch_score(const CUtensorMap& tmap_k, const CUtensorMap& tmap_q,
 // Shared-memory bytes the scoring kernel needs for a mode/topk.
 size_t score_smem_bytes(int mode, int topk);
 
-// One CTA per row: merge unit candidates (FinishParams::scores == null) or
-// select from a dense score matrix; then sort, map and write.
+// One CTA per row: merge unit candidates (FinishParams::scores and shard_raw
+// null), select from a dense score matrix (scores set) or from the union of
+// context-shard lists (shard_raw set); then sort, map and write.
 cudaError_t launch_finish(const FinishParams& p, cudaStream_t stream);
 
-// Checks 0 <= start <= end <= width for every row of a bare score matrix.
+// Checks 0 <= start <= end <= width for every row, and 0 <= row_req < num_req
+// when row_req is given.
 cudaError_t launch_validate_windows(const int32_t* row_start, const int32_t* row_end, int32_t rows,
-                                    int64_t width, PlanHeader* hdr, cudaStream_t stream);
+                                    int64_t width, PlanHeader* hdr, cudaStream_t stream,
+                                    const int32_t* row_req = nullptr, int32_t num_req = 0);
 
 // Context-tiled comparison path: windows of one chunk, and the per-chunk
 // merge into each row's running TopK (writing the outputs after the last).

@@ -63,14 +63,15 @@ struct SelSegments {
 // plus, with NREG > 0, the NREG append regions whose counts are in reg_cnt
 // (shared memory) -- to the K largest, stored in buf[0, min(n, K)); *cnt_s and,
 // when keys were dropped, *tau_s (the K-th largest key's radix prefix, a lower
-// bound of every kept key) are updated.  All keys are distinct.  CAP is the
-// buffer's capacity.
+// bound of every kept key) are updated.  All keys are distinct; keys that are
+// not (a list that names a position twice) leave the kept count off, which is
+// reported as err_code.  CAP is the buffer's capacity.
 template <int NT, int CAP, int NREG = 0>
 __device__ __noinline__ void sel_compact(uint64_t* buf, uint32_t* cnt_s, uint64_t* tau_s,
                                          uint32_t* hist, uint32_t* bc, uint32_t K, int tid,
                                          uint32_t bar_id, PlanHeader* hdr,
                                          const uint32_t* reg_cnt = nullptr, uint32_t reg_base = 0,
-                                         uint32_t reg_stride = 0) {
+                                         uint32_t reg_stride = 0, uint32_t err_code = kErrInternal) {
   SelSegments<NREG> sg;
   sg.kept = *(volatile uint32_t*)cnt_s;
   uint32_t n = sg.kept;
@@ -186,7 +187,7 @@ __device__ __noinline__ void sel_compact(uint64_t* buf, uint32_t* cnt_s, uint64_
   }
   if (tid == 0) {
     const uint32_t expect = n > K ? K : n;
-    if (bc[3] != expect) raise_status(hdr, kErrInternal, 200);
+    if (bc[3] != expect) raise_status(hdr, err_code, 200);
     *cnt_s = expect;
     if (n > K) *tau_s = prefix;
   }

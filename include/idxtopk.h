@@ -310,6 +310,59 @@ int idx_topk_set_timing(int32_t enable);
 int idx_topk_last_timings(float* ms4);
 
 /*
+ * Context-parallel pieces ("[AMD][DSv4] Add experimental AITER FP4 streaming
+ * TopK", sglang#38101, Changes: context-parallel paths; "[FlyDSL][DSv4]
+ * Prototype FP4 MQA streaming TopK", ROCm/aiter#5282, Changes: merge split
+ * candidates exactly).  A context partition [c_0, c_1), [c_1, c_2), ... of the
+ * logical C4 positions is scored one shard at a time (each call may run where
+ * that shard's K pages live); the shards' lists, gathered into one
+ * [S, R, topk] pair of tensors by the caller, are merged exactly.  The merged
+ * outputs equal those of idx_topk_fp4_prefill on the same data, bit for bit.
+ *
+ * idx_topk_fp4_prefill_shard: every row whose whole window [start, end) is
+ * longer than topk is scored against the part of it inside [ctx_begin,
+ * ctx_end) only -- however short that part -- and emits that part's exact
+ * TopK, ordered by (score desc, position asc):
+ *   out_score    f32 [R, topk]  the scores (as the fused path computes them),
+ *                               NaN after the part's last position
+ *   out_raw_idx  i32 [R, topk]  logical C4 positions, -1 after the last one
+ * Rows whose whole window is at most topk long emit only -1 / NaN (the merge
+ * gives them the closed form).  Inputs, value domain and errors as
+ * idx_topk_fp4_prefill; ctx_begin < 0 or ctx_end < ctx_begin is
+ * IDX_ERR_INVALID_ARGUMENT.  Only the page entries and K pages under the
+ * clipped windows are read and checked.  On error out_raw_idx is -1 and
+ * out_score NaN.
+ */
+int idx_topk_fp4_prefill_shard(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                               const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
+                               const idx_tensor_t* weights, const idx_tensor_t* page_table,
+                               const idx_tensor_t* row_req, const idx_tensor_t* row_start,
+                               const idx_tensor_t* row_end, int32_t ctx_begin, int32_t ctx_end,
+                               int32_t topk, const idx_tensor_t* out_score,
+                               const idx_tensor_t* out_raw_idx, idx_stream_t stream);
+
+/*
+ * idx_topk_merge_shards: the exact TopK of each row over the union of its S
+ * shard lists (aiter#5282 Changes: exact merge of split candidates), then the
+ * short-row contract and the page mapping of idx_topk_fp4_prefill.
+ *   shard_score  f32 [S, R, topk]  shard s's out_score (S >= 1)
+ *   shard_raw    i32 [S, R, topk]  shard s's out_raw_idx (-1 = empty entry)
+ *   page_table, row_req, row_start, row_end  as for idx_topk_fp4_prefill
+ *   out_phys_slot, out_raw_idx (nullable)   as for idx_topk_fp4_prefill
+ * The shards must cover every window and be disjoint.  A listed position
+ * outside its row's window, a position listed twice among the emitted TopK, or
+ * a row whose lists hold fewer than topk positions although its window is
+ * longer than topk returns IDX_ERR_INVALID_METADATA (as do bad row metadata);
+ * unsupported topk IDX_ERR_UNSUPPORTED; outputs -1 on every error.  Scratch:
+ * one status word.
+ */
+int idx_topk_merge_shards(const idx_tensor_t* shard_score, const idx_tensor_t* shard_raw,
+                          const idx_tensor_t* page_table, const idx_tensor_t* row_req,
+                          const idx_tensor_t* row_start, const idx_tensor_t* row_end,
+                          int32_t topk, const idx_tensor_t* out_phys_slot,
+                          const idx_tensor_t* out_raw_idx, idx_stream_t stream);
+
+/*
  * Context-tiled comparison path (an ablation of the fused design: "[FlyDSL]
  * [DSv4] Prototype FP4 MQA streaming TopK", ROCm/aiter#5282, Changes, names a
  * bounded context-tiled fallback).  The same operation and outputs as
