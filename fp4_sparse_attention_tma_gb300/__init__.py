@@ -23,6 +23,7 @@ __all__ = ["IdxError", "SUPPORTED_K", "idx_topk_fp4_prefill", "idx_topk_fp4_pref
            "idx_topk_fp4_prefill_host",
            "idx_topk_fp4_prefill_async", "idx_topk_fp4_prefill_paged",
            "idx_topk_fp4_prefill_shard", "idx_topk_merge_shards",
+           "idx_topk_fp4_prefill_mma_scales",
            "idx_dense_topk_fp4_prefill", "idx_tiled_topk_fp4_prefill",
            "idx_fp4_debug_scores", "idx_topk_select_scores", "idx_topk_supported_k",
            "idx_topk_status_string", "idx_topk_fp4_scratch_bytes", "idx_topk_scratch_high_water",
@@ -146,6 +147,19 @@ def idx_topk_fp4_prefill_noalloc(q_fp4, q_scale, k_cache_fp4, k_scale, weights, 
     code = lib.idx_topk_fp4_prefill_noalloc(*[_ref(d) for d in ds[:9]], int(topk), _ref(ds[9]),
                                             _ref(ds[10]), _stream(stream))
     return _check(code, "idx_topk_fp4_prefill_noalloc", raise_on_error)
+
+
+def idx_topk_fp4_prefill_mma_scales(q_fp4, q_scale, k_cache_fp4, k_scale_mma, weights,
+                                    page_table, row_req, row_start, row_end, topk, out_phys_slot,
+                                    out_raw_idx=None, stream=None, raise_on_error=True) -> int:
+    """idx_topk_fp4_prefill with the K scales [NP, 256] in the MMA's
+    scale-copy order: byte 8j + 4h + b of a page = scale b of slot 32h + j."""
+    lib = _lib.load()
+    ds = [_desc(t) for t in (q_fp4, q_scale, k_cache_fp4, k_scale_mma, weights, page_table,
+                             row_req, row_start, row_end, out_phys_slot, out_raw_idx)]
+    code = lib.idx_topk_fp4_prefill_mma_scales(*[_ref(d) for d in ds[:9]], int(topk),
+                                               _ref(ds[9]), _ref(ds[10]), _stream(stream))
+    return _check(code, "idx_topk_fp4_prefill_mma_scales", raise_on_error)
 
 
 def idx_topk_fp4_prefill_shard(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table,

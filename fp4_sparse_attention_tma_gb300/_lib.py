@@ -93,6 +93,9 @@ EXPORTS = {
     "idx_topk_fp4_prefill_noalloc": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
                                      [ctypes.c_int32, ctypes.POINTER(IdxTensor),
                                       ctypes.POINTER(IdxTensor), ctypes.c_void_p]),
+    "idx_topk_fp4_prefill_mma_scales": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
+                                        [ctypes.c_int32, ctypes.POINTER(IdxTensor),
+                                         ctypes.POINTER(IdxTensor), ctypes.c_void_p]),
     "idx_topk_fp4_prefill_shard": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
                                    [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                     ctypes.POINTER(IdxTensor), ctypes.POINTER(IdxTensor),

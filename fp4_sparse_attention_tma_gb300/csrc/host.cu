@@ -207,7 +207,8 @@ int check_inputs(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
                  const idx_tensor_t* k_cache_fp4, const idx_tensor_t* k_scale,
                  const idx_tensor_t* weights, const idx_tensor_t* page_table,
                  const idx_tensor_t* row_req, const idx_tensor_t* row_start,
-                 const idx_tensor_t* row_end, Sizes* sz, const idx_tensor_t* k_pages = nullptr) {
+                 const idx_tensor_t* row_end, Sizes* sz, const idx_tensor_t* k_pages = nullptr,
+                 bool k_scale_mma = false) {
   int st;
   if ((st = check_tensor(q_fp4, IDX_U8, 3))) return st;
   if ((st = check_tensor(q_scale, IDX_U8, 3))) return st;
@@ -217,7 +218,8 @@ int check_inputs(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
     if (k_pages->shape[1] != kPage * (kDimBytes + kNumSF)) return IDX_ERR_UNSUPPORTED;
   } else {
     if ((st = check_tensor(k_cache_fp4, IDX_U8, 3))) return st;
-    if ((st = check_tensor(k_scale, IDX_U8, 3))) return st;
+    // K scales: [NP, 64 slots, 4], or [NP, 256] in the MMA's scale-copy order
+    if ((st = check_tensor(k_scale, IDX_U8, k_scale_mma ? 2 : 3))) return st;
   }
   if ((st = check_tensor(weights, IDX_F32, 2))) return st;
   if ((st = check_tensor(page_table, IDX_I32, 2))) return st;
@@ -232,8 +234,12 @@ int check_inputs(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
   const int64_t R = q_fp4->shape[0];
   if (q_scale->shape[0] != R || q_scale->shape[1] != kHeads || q_scale->shape[2] != kNumSF)
     return IDX_ERR_INVALID_ARGUMENT;
-  if (!k_pages && (k_scale->shape[0] != k_cache_fp4->shape[0] || k_scale->shape[1] != kPage ||
-                   k_scale->shape[2] != kNumSF))
+  if (!k_pages && k_scale_mma &&
+      (k_scale->shape[0] != k_cache_fp4->shape[0] || k_scale->shape[1] != kPage * kNumSF))
+    return IDX_ERR_INVALID_ARGUMENT;
+  if (!k_pages && !k_scale_mma &&
+      (k_scale->shape[0] != k_cache_fp4->shape[0] || k_scale->shape[1] != kPage ||
+       k_scale->shape[2] != kNumSF))
     return IDX_ERR_INVALID_ARGUMENT;
   if (weights->shape[0] != R || weights->shape[1] != kHeads) return IDX_ERR_INVALID_ARGUMENT;
   if (row_req->shape[0] != R || row_start->shape[0] != R || row_end->shape[0] != R)
@@ -344,6 +350,7 @@ struct Call {
   const idx_tensor_t *scores, *logits;      // dense / debug score outputs
   Path path;
   const idx_tensor_t* k_pages = nullptr;    // page-interleaved K cache (replaces the two K tensors)
+  bool k_scale_mma = false;                 // k_scale [NP, 256] in the MMA's scale-copy order
 };
 
 // Where the scorer finds a page's codes and scales for a call.
@@ -408,7 +415,7 @@ int run(const Call& c, cudaStream_t stream) {
   if (prefill && !topk_supported(c.topk)) return fail(IDX_ERR_UNSUPPORTED);
   Sizes sz;
   st = check_inputs(c.q_fp4, c.q_scale, c.k_cache_fp4, c.k_scale, c.weights, c.page_table,
-                    c.row_req, c.row_start, c.row_end, &sz, c.k_pages);
+                    c.row_req, c.row_start, c.row_end, &sz, c.k_pages, c.k_scale_mma);
   if (st) return fail(st);
   int64_t score_stride = 0, logits_stride = 0, check_end = 0;
   if (c.path != Path::kFused && c.scores) {
@@ -493,6 +500,7 @@ int run(const Call& c, cudaStream_t stream) {
   sp.q_scale = (const uint8_t*)c.q_scale->data;
   sp.k_scale = ks.scales;
   sp.k_scale_stride = ks.scale_stride_words;
+  sp.k_scale_mma = c.k_scale_mma ? 1 : 0;
   sp.weights = (const float*)c.weights->data;
   sp.page_table = pp.page_table;
   sp.row_start = pp.row_start;
@@ -1433,6 +1441,19 @@ int idx_topk_fp4_prefill_paged(const idx_tensor_t* q_fp4, const idx_tensor_t* q_
                                const idx_tensor_t* out_raw_idx, idx_stream_t stream) {
   Call c{q_fp4, q_scale, nullptr, nullptr, weights, page_table, row_req, row_start, row_end,
          topk, out_phys_slot, out_raw_idx, nullptr, nullptr, Path::kFused, k_pages};
+  return run(c, (cudaStream_t)stream);
+}
+
+int idx_topk_fp4_prefill_mma_scales(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                                    const idx_tensor_t* k_cache_fp4,
+                                    const idx_tensor_t* k_scale_mma, const idx_tensor_t* weights,
+                                    const idx_tensor_t* page_table, const idx_tensor_t* row_req,
+                                    const idx_tensor_t* row_start, const idx_tensor_t* row_end,
+                                    int32_t topk, const idx_tensor_t* out_phys_slot,
+                                    const idx_tensor_t* out_raw_idx, idx_stream_t stream) {
+  Call c{q_fp4, q_scale, k_cache_fp4, k_scale_mma, weights, page_table, row_req, row_start,
+         row_end, topk, out_phys_slot, out_raw_idx, nullptr, nullptr, Path::kFused};
+  c.k_scale_mma = true;
   return run(c, (cudaStream_t)stream);
 }
 

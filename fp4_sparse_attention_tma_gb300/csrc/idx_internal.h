@@ -141,6 +141,9 @@ struct ScoreParams {
   const uint8_t* q_scale;
   const uint8_t* k_scale;    // page p's 64 scale words start at word p * k_scale_stride
   int64_t k_scale_stride;    // 32-bit words between consecutive pages' scales
+  int32_t k_scale_mma;       // 0: word s = slot s's 4 scales; 1: the MMA's scale-copy
+                             // order, word 2j + h = slot 32h + j's 4 scales
+  int32_t pad0;
   const float* weights;
   const int32_t* page_table;
   const int32_t* row_start;

@@ -490,10 +490,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto load_scales = [&](int32_t pg0, int32_t pg1, uint32_t (&w)[4]) {
         const bool v0 = pg0 >= 0 && pg0 < p.num_pages, v1 = pg1 >= 0 && pg1 < p.num_pages;
-        w[0] = v0 ? kscale[(int64_t)pg0 * p.k_scale_stride + lane] : 0u;
-        w[1] = v0 ? kscale[(int64_t)pg0 * p.k_scale_stride + 32 + lane] : 0u;
-        w[2] = v1 ? kscale[(int64_t)pg1 * p.k_scale_stride + lane] : 0u;
-        w[3] = v1 ? kscale[(int64_t)pg1 * p.k_scale_stride + 32 + lane] : 0u;
+        if (p.k_scale_mma) {
+          // already in copy order: slots lane and 32 + lane are one 8-byte word
+          const uint2 a = v0 ? *reinterpret_cast<const uint2*>(
+                                   kscale + (int64_t)pg0 * p.k_scale_stride + 2 * lane)
+                             : make_uint2(0u, 0u);
+          const uint2 b = v1 ? *reinterpret_cast<const uint2*>(
+                                   kscale + (int64_t)pg1 * p.k_scale_stride + 2 * lane)
+                             : make_uint2(0u, 0u);
+          w[0] = a.x;
+          w[1] = a.y;
+          w[2] = b.x;
+          w[3] = b.y;
+        } else {
+          w[0] = v0 ? kscale[(int64_t)pg0 * p.k_scale_stride + lane] : 0u;
+          w[1] = v0 ? kscale[(int64_t)pg0 * p.k_scale_stride + 32 + lane] : 0u;
+          w[2] = v1 ? kscale[(int64_t)pg1 * p.k_scale_stride + lane] : 0u;
+          w[3] = v1 ? kscale[(int64_t)pg1 * p.k_scale_stride + 32 + lane] : 0u;
+        }
       };
       uint32_t wnext[4] = {0u, 0u, 0u, 0u};
       bool have_next = false;

@@ -221,6 +221,15 @@ def config(idx: int) -> Problem:
     raise ValueError(f"no workload {idx}")
 
 
+def k_scale_mma_order(k_scale: np.ndarray) -> np.ndarray:
+    """A [NP, 64, 4] K-scale array rearranged (a pure permutation of bytes) into
+    the [NP, 256] order of idx_topk_fp4_prefill_mma_scales: byte 8j + 4h + b of
+    a page holds scale b of slot 32h + j."""
+    npg = k_scale.shape[0]
+    return np.ascontiguousarray(
+        np.asarray(k_scale).reshape(npg, 2, 32, 4).transpose(0, 2, 1, 3).reshape(npg, 256))
+
+
 def small_problem(seed: int = 7, topk: int = 512, c4_lens=(1500, 2600, 700),
                   rows_per_req=(5, 9, 3), start_offsets=True) -> Problem:
     """A small ragged multi-request case the oracle finishes in well under a second.

@@ -161,6 +161,29 @@ int idx_topk_fp4_prefill_paged(const idx_tensor_t* q_fp4, const idx_tensor_t* q_
                                const idx_tensor_t* out_raw_idx, idx_stream_t stream);
 
 /*
+ * idx_topk_fp4_prefill with the K cache's scales pre-arranged in the order in
+ * which the block-scaled MMA's scale copy reads them (the pre-shuffled scale
+ * input named as follow-up work in "[FlyDSL][DSv4] Prototype FP4 MQA streaming
+ * TopK", ROCm/aiter#5282, Scope; here the layout of sm_103a's 32x128b scale
+ * copy into tensor memory instead of the AMD matrix-core layout):
+ *   k_scale_mma u8 [NP, 256]  byte 8*j + 4*h + b of page p = scale b (D
+ *                             elements 32b .. 32b+31) of slot 32*h + j of page
+ *                             p, for j < 32, h < 2, b < 4; i.e. the page's
+ *                             slot words reordered j, 32+j, j+1, 33+j, ...
+ * A cache writer that stores its scales this way spares the scorer the
+ * rearrangement; each producer lane then reads one 8-byte word per page.
+ * Every other argument, the value domain, the results and the errors are those
+ * of idx_topk_fp4_prefill; the outputs are identical for the same data.
+ */
+int idx_topk_fp4_prefill_mma_scales(const idx_tensor_t* q_fp4, const idx_tensor_t* q_scale,
+                                    const idx_tensor_t* k_cache_fp4,
+                                    const idx_tensor_t* k_scale_mma, const idx_tensor_t* weights,
+                                    const idx_tensor_t* page_table, const idx_tensor_t* row_req,
+                                    const idx_tensor_t* row_start, const idx_tensor_t* row_end,
+                                    int32_t topk, const idx_tensor_t* out_phys_slot,
+                                    const idx_tensor_t* out_raw_idx, idx_stream_t stream);
+
+/*
  * idx_topk_fp4_prefill on tensors in host memory (no counterpart on the
  * pages: it serves callers whose query block, K cache and metadata sit
  * in host memory, and it is the end-to-end form of the operation, host copies

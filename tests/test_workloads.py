@@ -96,3 +96,17 @@ def test_tiny_workload_has_exact_ties():
     keys = np.concatenate([slots, scales], axis=1)
     _, counts = np.unique(keys, axis=0, return_counts=True)
     assert (counts >= 2).sum() >= 64
+
+
+def test_k_scale_mma_order_is_the_documented_permutation():
+    # byte 8j + 4h + b of a page = scale b of slot 32h + j (a permutation of
+    # each page's 256 bytes)
+    k = np.random.default_rng(5).integers(0, 256, size=(3, 64, 4), dtype=np.uint8)
+    o = inputs.k_scale_mma_order(k)
+    assert o.shape == (3, 256) and o.flags["C_CONTIGUOUS"]
+    for p in range(3):
+        for j in range(32):
+            for h in range(2):
+                for b in range(4):
+                    assert o[p, 8 * j + 4 * h + b] == k[p, 32 * h + j, b]
+        assert sorted(o[p].tolist()) == sorted(k[p].ravel().tolist())
