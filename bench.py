@@ -60,7 +60,30 @@ def parse_args():
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the per-workload lines and the fresh-process repeats")
+    ap.add_argument("--child-pairs", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args()
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the CPU baseline."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "hardware")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine() or "unknown"
 
 
 def dist_env():
@@ -201,10 +224,121 @@ def cpu_baseline(p, seconds: float):
     dt = time.perf_counter() - t0
     flop = float(p.lengths()[pick].sum()) * 2 * 64 * 128
     return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(),
-            "kind": "oracle",
+            "cpu_model": cpu_model(), "kind": "oracle",
             "sample": f"{n} of {len(scored)} scored rows (evenly spaced), full windows, "
                       f"{dt:.1f} s wall",
             "seconds": dt}
+
+
+def timed_pairs(m, dev, p, n_warm, n_pairs, flush):
+    """Alternating dense-then-TopK / fused calls on one stream (L2 flushed before
+    each), n_warm pairs untimed then n_pairs timed with CUDA events; the two
+    medians and whether the outputs were identical."""
+    import torch
+    R, K = p.rows, p.topk
+    phys = torch.empty((R, K), dtype=torch.int32, device="cuda")
+    raw = torch.empty((R, K), dtype=torch.int32, device="cuda")
+    d_phys = torch.empty_like(phys)
+    d_raw = torch.empty_like(raw)
+    ws = torch.empty((R, p.max_end()), dtype=torch.float32, device="cuda")
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+
+    def fused():
+        m.idx_topk_fp4_prefill(**dev, topk=K, out_phys_slot=phys, out_raw_idx=raw)
+
+    def dense():
+        m.idx_dense_topk_fp4_prefill(**dev, topk=K, out_phys_slot=d_phys, out_raw_idx=d_raw,
+                                     score_workspace=ws)
+
+    f_ms, d_ms = [], []
+    for i in range(n_warm + n_pairs):
+        for fn, acc in ((dense, d_ms), (fused, f_ms)):
+            flush.zero_()
+            ev0.record()
+            fn()
+            ev1.record()
+            ev1.synchronize()
+            if i >= n_warm:
+                acc.append(ev0.elapsed_time(ev1))
+    same = bool(torch.equal(d_raw, raw) and torch.equal(d_phys, phys))
+    return {"fused_ms_median": statistics.median(f_ms), "dense_ms_median": statistics.median(d_ms),
+            "indices_identical": same, "score_storage_bytes": ws.numel() * 4}
+
+
+def child_pairs(args):
+    """One fresh process of the repeated measurement: 5 warm-up and
+    args.pairs timed dense/fused pairs on the workload; prints one JSON line."""
+    import numpy as np
+    import torch
+    import fp4_sparse_attention_tma_gb300 as m
+    from fp4_sparse_attention_tma_gb300 import inputs
+    torch.cuda.set_device(0)
+    p = inputs.config(args.config)
+    dev = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).cuda()
+           for k in ("q_fp4", "q_scale", "k_cache_fp4", "k_scale", "weights", "page_table",
+                     "row_req", "row_start", "row_end")}
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    print(json.dumps(timed_pairs(m, dev, p, 5, args.pairs, flush)), flush=True)
+
+
+def fresh_processes(args, n=3):
+    """The dense/fused pair measurement repeated in n fresh processes (each 5
+    warm-up + args.pairs timed pairs); the median over processes of each
+    process's median."""
+    runs = []
+    for _ in range(n):
+        out = subprocess.run([sys.executable, os.path.abspath(__file__), "--child-pairs",
+                              "--config", str(args.config), "--pairs", str(args.pairs)],
+                             capture_output=True, text=True, timeout=600)
+        if out.returncode != 0:
+            raise RuntimeError("fresh-process measurement failed:\n" + out.stderr[-2000:])
+        runs.append(json.loads(out.stdout.strip().splitlines()[-1]))
+    return {"processes": n, "warmup_pairs": 5, "timed_pairs": args.pairs,
+            "fused_ms_median": statistics.median(r["fused_ms_median"] for r in runs),
+            "dense_ms_median": statistics.median(r["dense_ms_median"] for r in runs),
+            "indices_identical": all(r["indices_identical"] for r in runs),
+            "per_process": [{"fused_ms": r["fused_ms_median"], "dense_ms": r["dense_ms_median"]}
+                            for r in runs]}
+
+
+def other_workloads(m, local, flush, cfgs=(0, 1, 2, 4), steps=10, warm=3):
+    """The other configurations through the same call, timed in this run: per
+    workload the call's mean time (L2 flushed before each call), its
+    algorithmic TFLOP/s, the scorer's time and the scratch a call takes."""
+    import numpy as np
+    import torch
+    from fp4_sparse_attention_tma_gb300 import inputs
+    out = []
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    for c in cfgs:
+        p = inputs.config(c)
+        dev = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).cuda()
+               for k in ("q_fp4", "q_scale", "k_cache_fp4", "k_scale", "weights", "page_table",
+                         "row_req", "row_start", "row_end")}
+        phys = torch.empty((p.rows, p.topk), dtype=torch.int32, device="cuda")
+        raw = torch.empty_like(phys)
+        ms, sc = [], []
+        for i in range(warm + steps):
+            flush.zero_()
+            ev0.record()
+            m.idx_topk_fp4_prefill(**dev, topk=p.topk, out_phys_slot=phys, out_raw_idx=raw)
+            ev1.record()
+            ev1.synchronize()
+            if i >= warm:
+                ms.append(ev0.elapsed_time(ev1))
+                sc.append(m.idx_topk_last_timings()["score_ms"])
+        flop = float(p.algorithmic_flop())
+        call = statistics.mean(ms)
+        out.append({"workload": p.name, "rows": p.rows, "topk": p.topk,
+                    "scored_pairs": p.scored_pairs(), "algorithmic_flop": flop,
+                    "call_ms": call, "tflops": flop / (call * 1e-3) / 1e12,
+                    "score_ms": statistics.mean(sc),
+                    "scratch_bytes": m.idx_topk_fp4_scratch_bytes(p.rows, p.topk, local),
+                    "steps": steps})
+        del dev, phys, raw
+    return out
 
 
 def run_reference(args):
@@ -243,7 +377,7 @@ def run_reference(args):
             "config": {"workload": p.name, "rows": p.rows, "c4_context": p.max_end(),
                        "topk": p.topk},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(),
-                             "kind": "oracle", "sample": sample},
+                             "cpu_model": cpu_model(), "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -251,6 +385,9 @@ def run_reference(args):
 
 def main():
     args = parse_args()
+    if args.child_pairs:
+        child_pairs(args)
+        return
     if args.impl == "reference":
         run_reference(args)
         return
@@ -383,31 +520,12 @@ def main():
                        "dense_scores_bytes": m.dense_score_bytes(R, p.max_end())}
 
     if not args.no_dense:
-        ws = torch.empty((R, p.max_end()), dtype=torch.float32, device="cuda")
-        d_phys = torch.empty_like(phys)
-        d_raw = torch.empty_like(raw)
-
-        def dense():
-            m.idx_dense_topk_fp4_prefill(**dev, topk=K, out_phys_slot=d_phys, out_raw_idx=d_raw,
-                                         score_workspace=ws)
-
-        f_ms, d_ms = [], []
-        for i in range(5 + args.pairs):
-            for fn, acc in ((dense, d_ms), (fused, f_ms)):
-                flush.zero_()
-                ev0.record()
-                fn()
-                ev1.record()
-                ev1.synchronize()
-                if i >= 5:
-                    acc.append(ev0.elapsed_time(ev1))
-        same = bool(torch.equal(d_raw, raw) and torch.equal(d_phys, phys))
-        line["dense_topk"] = {"ms_median": statistics.median(d_ms),
-                              "fused_ms_median": statistics.median(f_ms),
-                              "speedup": statistics.median(d_ms) / statistics.median(f_ms),
-                              "pairs": args.pairs, "indices_identical": same,
-                              "score_storage_bytes": ws.numel() * 4}
-        del ws
+        pairs = timed_pairs(m, dev, p, 5, args.pairs, flush)
+        line["dense_topk"] = {"ms_median": pairs["dense_ms_median"],
+                              "fused_ms_median": pairs["fused_ms_median"],
+                              "speedup": pairs["dense_ms_median"] / pairs["fused_ms_median"],
+                              "pairs": args.pairs, "indices_identical": pairs["indices_identical"],
+                              "score_storage_bytes": pairs["score_storage_bytes"]}
 
     if not args.no_dense:
         # context-tiled comparison path: bounded fp32 chunks of 16384 positions
@@ -429,6 +547,12 @@ def main():
                               "indices_identical": bool(torch.equal(t_raw, raw) and
                                                         torch.equal(t_phys, phys))}
 
+    if rank == 0 and world == 1 and not args.no_extra:
+        m.idx_topk_set_timing(True)
+        line["workloads"] = other_workloads(m, local, flush)
+        m.idx_topk_set_timing(False)
+        if not args.no_dense:
+            line["fresh_processes"] = fresh_processes(args)
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(p, args.cpu_seconds)
     if rank == 0:

@@ -78,6 +78,7 @@ def test_reference_arm_prints_one_line_on_rank_zero():
     assert d["steps"] == 2 and d["warmup"] == 3 and d["higher_is_better"] is True
     assert d["config"]["workload"] == "tiny-R32-S4096-K512" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert isinstance(d["cpu_baseline"]["cpu_model"], str) and d["cpu_baseline"]["cpu_model"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["vs_baseline"] is None          # the pages give no time for this workload
 
