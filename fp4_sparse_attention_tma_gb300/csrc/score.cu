@@ -232,6 +232,38 @@ __device__ __forceinline__ float head_sum_final(const uint64_t (&acc)[4]) {
   return (t.x + t.y) + 0.0f;
 }
 
+// The select step of one slot: the 64-bit order key (32-bit score key in the
+// high word, ~position in the low word) is appended to the warp's region at
+// wreg_s (shared address) when pass_in is set and the key is at least tau;
+// *wcnt counts the region's keys.  One ballot, a predicated store and the
+// count update, no branch.  The score key here is sb ^ (sign(sb) ? ~0 :
+// 0x80000000): the order key of a finite score (every accepted call's scores
+// are finite; the NaN rule of score_key needs no test here).
+__device__ __forceinline__ void append_if(uint32_t& wcnt, uint32_t wreg_s, float sc, uint32_t lo,
+                                          uint64_t tau, uint32_t pass_in, uint32_t lt_mask) {
+  asm volatile(
+      "{\n\t.reg .b64 key;\n\t.reg .pred p, q;\n\t.reg .b32 sb, sh, k, m, off, c, a;\n\t"
+      "mov.b32 sb, %2;\n\t"
+      "shr.s32 sh, sb, 31;\n\t"
+      "or.b32 sh, sh, 0x80000000;\n\t"
+      "xor.b32 k, sb, sh;\n\t"
+      "mov.b64 key, {%3, k};\n\t"
+      "setp.ne.u32 q, %5, 0;\n\t"
+      "setp.ge.and.u64 p, key, %4, q;\n\t"
+      "vote.sync.ballot.b32 m, p, 0xffffffff;\n\t"
+      "and.b32 off, m, %6;\n\t"
+      "popc.b32 off, off;\n\t"
+      "add.u32 off, off, %0;\n\t"
+      "shl.b32 off, off, 3;\n\t"
+      "add.u32 a, off, %1;\n\t"
+      "@p st.shared.b64 [a], key;\n\t"
+      "popc.b32 c, m;\n\t"
+      "add.u32 %0, %0, c;\n\t}"
+      : "+r"(wcnt)
+      : "r"(wreg_s), "f"(sc), "r"(lo), "l"(tau), "r"(pass_in), "r"(lt_mask)
+      : "memory");
+}
+
 // Collective over a row's four epilogue warps (named barrier bar_id, 128
 // threads): keeps the row's TOPK largest keys over the four regions (region w
 // at buf + w * warp_region(TOPK), holding wc_s[w] keys) and compacts each region
@@ -725,34 +757,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (scale_bytes_over(qsf) != 0u || weight_out_of_domain(wb))
               raise_status(hdr, kErrInvalidValue, 323);
           }
-          uint32_t thi = 0, tlo = 0;  // threshold key (score key, ~index)
-          uint32_t wcnt = 0;          // keys in this warp's append region
+          uint64_t tau = 0;    // threshold key: appended keys are >= tau
+          uint32_t wcnt = 0;   // keys in this warp's append region
           uint64_t* wreg = cand + (uint32_t)qd * warp_region(TOPK);
+          const uint32_t wreg_s = smem_u32(wreg);
+          const uint32_t lt_mask = (1u << lane) - 1u;
           if constexpr (MODE == kModeSelect) {
             if (tg == 0) *tau_s = 0ull;
             bar_sync(bar_id, kEpiThreads);
           }
           const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16) + kColAcc + 64u * g;
           int check_in = kCheckTiles;  // tiles until the next over-limit check
-          // The reduction of a tile's sums to its score and the select step
-          // run one tile late, right after the next tile's first TMEM load is
-          // issued, so that their dependent chain overlaps that load and the
-          // next tile's arithmetic.  The first call of a unit is a no-op.
-          uint64_t pacc[4] = {0ull, 0ull, 0ull, 0ull};
+          // A tile's score is reduced at the end of the tile; its select step
+          // runs one tile late, right after the next tile's first TMEM load is
+          // issued, so that its dependent chain overlaps that load.  The first
+          // call of a unit is a no-op (pwin false).
+          float psc = 0.f;
           int32_t pslot = 0;
           bool pwin = false;
           auto tail = [&]() {
-            const float sc = head_sum_final(pacc);
             if constexpr (MODE == kModeDense) {
-              if (pwin) p.dense_out[row * p.dense_stride + (pslot - p.dense_col0)] = sc;
+              if (pwin) p.dense_out[row * p.dense_stride + (pslot - p.dense_col0)] = psc;
             } else {
-              // cheap 32-bit test first; the low word only decides exact ties
-              const uint32_t k32 = score_key(sc);
-              const bool pass = pwin & ((k32 > thi) | ((k32 == thi) & (~(uint32_t)pslot >= tlo)));
-              const uint64_t key = ((uint64_t)k32 << 32) | (uint64_t)(~(uint32_t)pslot);
-              const uint32_t m = __ballot_sync(0xffffffffu, pass);
-              if (pass) wreg[wcnt + (uint32_t)__popc(m & ((1u << lane) - 1u))] = key;
-              wcnt += (uint32_t)__popc(m);
+              append_if(wcnt, wreg_s, psc, ~(uint32_t)pslot, tau, (uint32_t)pwin, lt_mask);
             }
           };
           for (int t = uv.u.t_begin; t < uv.u.t_end; ++t) {
@@ -799,8 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++acc_use;
             dump(xb, 48);
             head_sum_part<24>(xb, w2, acc);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) pacc[k] = acc[k];
+            psc = head_sum_final(acc);
             pslot = slot;
             pwin = in_win;
             if constexpr (MODE == kModeSelect) {
@@ -813,9 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (bar_red_or(bar_id, kEpiThreads, over)) {
                   wcnt = sel_compact_regions<TOPK>(cand, wc_s, tau_s, hist, bc, wcnt, qd, lane,
                                                    bar_id, hdr);
-                  const uint64_t tk = *(volatile uint64_t*)tau_s;
-                  thi = (uint32_t)(tk >> 32);
-                  tlo = (uint32_t)(tk & 0xffffffffu);
+                  tau = *(volatile uint64_t*)tau_s;
                   load_w2();  // the weights are not kept live across the compaction
                 }
               }
