@@ -4,7 +4,8 @@
 // A row keeps a buffer of 64-bit order keys (see order_key) that are >= its
 // threshold tau.  Threads append passing keys with warp-aggregated atomics;
 // when the count gets close to the capacity, the group runs a radix select
-// (8-bit digits, most significant first, with early exit) that finds a
+// (8-bit windows, most significant first, the first one starting at the
+// highest bit in which the keys differ, with early exit) that finds a
 // threshold T with exactly topk keys >= T, compacts the buffer to those keys
 // and raises tau to T.  Because the composite key includes the logical index,
 // keys of one row are distinct and the selection is exact.  This follows the
@@ -112,11 +113,16 @@ __device__ __noinline__ void sel_compact(uint64_t* buf, uint32_t* cnt_s, uint64_
     }
     bar_sync(bar_id, NT);  // the words are read before the histogram is cleared
     const int top = 63 - __clzll((long long)(kand ^ kor));
-    int shift = (top >> 3) << 3;
-    uint64_t pmask = shift == 56 ? 0ull : (~0ull << (shift + 8));
+    // the first 8-bit window starts at the highest differing bit, so that it
+    // splits the keys 256 ways instead of the 2 or 3 ways a byte-aligned window
+    // gives keys of nearly equal scores (fewer passes, and the histogram's
+    // shared-memory atomics spread over many bins)
+    int shift = top >= 7 ? top - 7 : 0;
+    uint64_t pmask = shift >= 56 ? 0ull : (~0ull << (shift + 8));
     prefix = kand & pmask;
     uint32_t need = K;
-    for (; shift >= 0; shift -= 8) {
+    for (; shift > -8; shift -= 8) {
+      if (shift < 0) shift = 0;  // the last window overlaps bits already resolved
       for (int b2 = tid; b2 < 256; b2 += NT) hist[b2] = 0;
       bar_sync(bar_id, NT);
       for (uint32_t i = tid; i < n; i += NT) {
@@ -153,7 +159,7 @@ __device__ __noinline__ void sel_compact(uint64_t* buf, uint32_t* cnt_s, uint64_
       need -= ab;
       prefix |= (uint64_t)d << shift;
       pmask |= (uint64_t)0xffu << shift;
-      if (cd == need) break;
+      if (cd == need || shift == 0) break;
     }
   }
   // Keep the keys >= prefix, written in order of the scan to buf[0, ...):

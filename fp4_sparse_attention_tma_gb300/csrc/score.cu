@@ -306,12 +306,17 @@ __device__ __noinline__ uint32_t sel_compact_regions(uint64_t* buf, const uint32
   }
   bar_sync(bar_id, kEpiThreads);
   const int top = 63 - __clzll((long long)(kand ^ kor));
-  int shift = (top >> 3) << 3;
-  uint64_t pmask = shift == 56 ? 0ull : (~0ull << (shift + 8));
+  // the first 8-bit window starts at the highest differing bit, so that it
+  // splits the keys 256 ways instead of the 2 or 3 ways a byte-aligned window
+  // gives keys of nearly equal scores (fewer passes, and the histogram's
+  // shared-memory atomics spread over many bins)
+  int shift = top >= 7 ? top - 7 : 0;
+  uint64_t pmask = shift >= 56 ? 0ull : (~0ull << (shift + 8));
   uint64_t prefix = kand & pmask;
   uint32_t need = (uint32_t)TOPK;
   const int tg = qd * 32 + lane;
-  for (; shift >= 0; shift -= 8) {
+  for (; shift > -8; shift -= 8) {
+    if (shift < 0) shift = 0;  // the last window overlaps bits already resolved
     for (int b2 = tg; b2 < 256; b2 += kEpiThreads) hist[b2] = 0;
     bar_sync(bar_id, kEpiThreads);
     for (uint32_t i = lane; i < my_cnt; i += 32) {
@@ -348,7 +353,7 @@ __device__ __noinline__ uint32_t sel_compact_regions(uint64_t* buf, const uint32
     need -= ab;
     prefix |= (uint64_t)d << shift;
     pmask |= (uint64_t)0xffu << shift;
-    if (cd == need) break;
+    if (cd == need || shift == 0) break;
   }
   // in place: a kept key moves to an index no higher than the one it was read
   // from, and a chunk is read before any of its slots is written
