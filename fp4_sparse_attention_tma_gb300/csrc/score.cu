@@ -98,12 +98,13 @@ constexpr uint32_t kIdescK1 = idesc_mxf4(128, kAccCols, 2);
 // Per-row candidate buffer of order keys, split into one region per epilogue
 // warp of the row (warp_region keys each).  A warp appends its passing keys to
 // its own region, counting in a register (no shared-memory atomics).  Every
-// kCheckTiles tiles the row's warps vote; when a region has fewer than
-// kCheckTiles * 32 entries free, the group finds the threshold that keeps
-// exactly topk keys over all four regions and each warp compacts its own
-// region in place.  A region never has to hold more than topk survivors plus
+// kCheckTiles tiles the warps of the block's scored rows vote (named barrier
+// kBarVote); when a region of any row has fewer than kCheckTiles * 32 entries
+// free, each row's group finds the threshold that keeps exactly topk keys over
+// its four regions and each warp compacts its own region in place.  A region never has to hold more than topk survivors plus
 // one check window of appends.
 constexpr int kCheckTiles = 12;
+constexpr uint32_t kBarVote = 4;  // named barrier of the compaction vote (1..3: row groups)
 // The candidate buffers take all shared memory the pipeline leaves free.
 constexpr uint32_t kMaxSmem = 227u * 1024u;
 constexpr uint32_t kCandCap = (kMaxSmem - 1024u - kOffCand) / (kRowsPerBlock * 8u) / 128u * 128u;
@@ -773,6 +774,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16) + kColAcc + 64u * g;
           int check_in = kCheckTiles;  // tiles until the next over-limit check
+          // scored rows of the block: their warps take part in the votes (every
+          // epilogue warp computes the same count from the same row windows)
+          uint32_t n_act = 0;
+          for (int j = 0; j < uv.b.nrows; ++j)
+            n_act += (p.row_end[uv.b.row0 + j] - p.row_start[uv.b.row0 + j]) > p.score_thr;
           // A tile's score is reduced at the end of the tile; its select step
           // runs one tile late, right after the next tile's first TMEM load is
           // issued, so that its dependent chain overlaps that load.  The first
@@ -841,7 +847,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 check_in = kCheckTiles;
                 const bool over = wcnt > warp_region(TOPK) - kCheckTiles * 32u;
                 if (lane == 0) wc_s[qd] = wcnt;  // visible to the group after the vote
-                if (bar_red_or(bar_id, kEpiThreads, over)) {
+                // one vote for the whole block: when any row needs it, every
+                // scored row compacts at the same tile, so that their pauses
+                // (each holds the accumulator handshake of all 12 warps) overlap
+                if (bar_red_or(kBarVote, n_act * kEpiThreads, over)) {
                   wcnt = sel_compact_regions<TOPK>(cand, wc_s, tau_s, hist, bc, wcnt, qd, lane,
                                                    bar_id, hdr);
                   tau = *(volatile uint64_t*)tau_s;
