@@ -20,6 +20,12 @@ CSRC = os.path.join(_HERE, "csrc")
 INCLUDE = os.path.join(_ROOT, "include")
 BUILD_DIR = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_HERE, "libidxtopk.so")
+# the range-checked variant (-DIDX_DEBUG_BOUNDS): every indexed scratch and
+# output access of the kernels is checked; an index outside its buffer fails
+# the call with IDX_ERR_INTERNAL instead of touching memory (a software stand-in
+# for a memory checker, run by the GPU tests on small cases)
+DEBUG_BUILD_DIR = os.path.join(_HERE, "_build_dbg")
+DEBUG_LIB_PATH = os.path.join(_HERE, "libidxtopk_dbg.so")
 SOURCES = ["host.cu", "plan.cu", "score.cu", "finish.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -42,17 +48,21 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile csrc/*.cu for sm_103a and link libidxtopk.so (no-op when fresh)."""
-    if (not force and os.path.exists(LIB_PATH)
-            and os.path.getmtime(LIB_PATH) >= _deps_mtime()):
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, debug_bounds: bool = False) -> str:
+    """Compile csrc/*.cu for sm_103a and link libidxtopk.so (no-op when fresh);
+    debug_bounds=True builds the range-checked libidxtopk_dbg.so instead."""
+    lib_path = DEBUG_LIB_PATH if debug_bounds else LIB_PATH
+    build_dir = DEBUG_BUILD_DIR if debug_bounds else BUILD_DIR
+    flags = NVCC_FLAGS + (["-DIDX_DEBUG_BOUNDS"] if debug_bounds else [])
+    if (not force and os.path.exists(lib_path)
+            and os.path.getmtime(lib_path) >= _deps_mtime()):
+        return lib_path
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-        cmd = [nvcc] + NVCC_FLAGS + ["-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
+        cmd = [nvcc] + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{res.stderr}")
@@ -62,13 +72,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, "-shared"] + ARCH + objs + ["-o", tmp]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 class IdxTensor(ctypes.Structure):

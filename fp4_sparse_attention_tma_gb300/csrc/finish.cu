@@ -27,6 +27,7 @@ constexpr int kFinGridCap = 2048;  // merging CTAs (rows strided over them)
 
 __device__ __forceinline__ int32_t map_phys(const int32_t* row_pt, int32_t raw) {
   if (raw < 0 || row_pt == nullptr) return -1;
+  // (the windows, hence raw / 64 < max_pages, were validated by the plan)
   const int64_t v = (int64_t)row_pt[raw >> 6] * kPage + (raw & (kPage - 1));
   return (int32_t)v;
 }
@@ -255,6 +256,7 @@ __device__ __forceinline__ void team_rows(const FinishParams& p, int64_t blk, Te
   const BlockInfo bi = p.blocks[p.row_block[r]];
   if (bi.n_units != 1) return;
   const int64_t slot = bi.slot0 + (r - bi.row0);
+  if (!IDX_IN_RANGE(slot >= 0 && slot < p.hdr->n_row_slots, p.hdr, 430)) return;
   const uint32_t n = min(p.cand_cnt[slot], (uint32_t)TOPK);
   const uint64_t* keys = p.cand_keys + slot * TOPK;
   uint64_t v[kTeamE];
@@ -392,7 +394,8 @@ __device__ __forceinline__ void finish_row(const FinishParams& p, int64_t r, Fin
     bool gathered = false;
     if (bi.n_units <= kFinThreads) {
       uint32_t c = 0;
-      if (tid < bi.n_units)
+      if (tid < bi.n_units &&
+          IDX_IN_RANGE(bi.slot0 + (int64_t)tid * bi.nrows + j < p.hdr->n_row_slots, p.hdr, 431))
         c = min(p.cand_cnt[bi.slot0 + (int64_t)tid * bi.nrows + j], (uint32_t)TOPK);
       const int lane = tid & 31, w = tid >> 5;
       uint32_t x = c;  // inclusive scan of the counts: lanes, then warps
@@ -431,6 +434,7 @@ __device__ __forceinline__ void finish_row(const FinishParams& p, int64_t r, Fin
     }
     for (int k = 0; !gathered && k < bi.n_units; ++k) {
       const int64_t slot = bi.slot0 + (int64_t)k * bi.nrows + j;
+      if (!IDX_IN_RANGE(slot < p.hdr->n_row_slots, p.hdr, 432)) break;
       const uint32_t n = min(p.cand_cnt[slot], (uint32_t)TOPK);
       const uint64_t* keys = p.cand_keys + slot * TOPK;
       for (uint32_t base = 0; base < n; base += kFinBatch) {

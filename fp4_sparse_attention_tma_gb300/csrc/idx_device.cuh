@@ -24,6 +24,21 @@ __device__ __forceinline__ uint32_t read_status(const PlanHeader* hdr) {
   return *(volatile const uint32_t*)&hdr->status;
 }
 
+// Software range checks of the debug build (compiled with -DIDX_DEBUG_BOUNDS;
+// it stands in for a memory checker): IDX_IN_RANGE(cond, hdr, site) is false,
+// and records kErrInternal with `site`, when an index is outside its buffer, so
+// that the caller skips the access and the call fails closed.  In the release
+// build it is the constant true and costs nothing.
+#ifdef IDX_DEBUG_BOUNDS
+__device__ __forceinline__ bool idx_in_range(bool ok, PlanHeader* hdr, uint32_t site) {
+  if (!ok) raise_status(hdr, kErrInternal, site);
+  return ok;
+}
+#define IDX_IN_RANGE(cond, hdr, site) ::idxk::idx_in_range((cond), (hdr), (site))
+#else
+#define IDX_IN_RANGE(cond, hdr, site) true
+#endif
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -278,6 +278,7 @@ __device__ __noinline__ uint32_t sel_compact_regions(uint64_t* buf, const uint32
                                                      int lane, uint32_t bar_id, PlanHeader* hdr) {
   constexpr uint32_t kQ = warp_region(TOPK);
   uint64_t* reg = buf + (uint32_t)qd * kQ;
+  if (!IDX_IN_RANGE(my_cnt <= kQ, hdr, 340)) my_cnt = kQ;
   uint32_t n = 0;
 #pragma unroll
   for (int w = 0; w < 4; ++w) n += ((volatile const uint32_t*)wc_s)[w];
@@ -364,7 +365,8 @@ __device__ __noinline__ uint32_t sel_compact_regions(uint64_t* buf, const uint32
     const uint64_t v = i < my_cnt ? reg[i] : 0ull;
     const bool keep = i < my_cnt && v >= prefix;
     const uint32_t m = __ballot_sync(0xffffffffu, keep);
-    if (keep) reg[kept + (uint32_t)__popc(m & ((1u << lane) - 1u))] = v;
+    const uint32_t at = kept + (uint32_t)__popc(m & ((1u << lane) - 1u));
+    if (keep && IDX_IN_RANGE(at < kQ, hdr, 341)) reg[at] = v;
     kept += (uint32_t)__popc(m);
     __syncwarp();
   }
@@ -735,8 +737,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(bar(kBarAccEmpty + b));
           ++acc_use;
         }
-        if (MODE == kModeSelect && valid && tg == 0)
-          p.cand_cnt[uv.b.slot0 + (int64_t)uv.u.k * uv.b.nrows + g] = 0;
+        if (MODE == kModeSelect && valid && tg == 0) {
+          const int64_t slot_idx = uv.b.slot0 + (int64_t)uv.u.k * uv.b.nrows + g;
+          if (IDX_IN_RANGE(slot_idx >= 0 && slot_idx < hdr->n_row_slots, hdr, 343))
+            p.cand_cnt[slot_idx] = 0;
+        }
       } else {
         if (!wait(bar(kBarQFull + qb), qpar, 320)) {
           ok = false;
@@ -788,9 +793,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool pwin = false;
           auto tail = [&]() {
             if constexpr (MODE == kModeDense) {
-              if (pwin) p.dense_out[row * p.dense_stride + (pslot - p.dense_col0)] = psc;
+              if (pwin && IDX_IN_RANGE((int64_t)pslot - p.dense_col0 >= 0 &&
+                                           (int64_t)pslot - p.dense_col0 < p.dense_stride,
+                                       hdr, 345))
+                p.dense_out[row * p.dense_stride + (pslot - p.dense_col0)] = psc;
             } else {
               append_if(wcnt, wreg_s, psc, ~(uint32_t)pslot, tau, (uint32_t)pwin, lt_mask);
+              // the region never holds more than its capacity
+              if (!IDX_IN_RANGE(wcnt <= warp_region(TOPK), hdr, 342)) wcnt = warp_region(TOPK);
             }
           };
           for (int t = uv.u.t_begin; t < uv.u.t_end; ++t) {
@@ -877,9 +887,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pre += w < qd ? c : 0u;
                 n += c;
               }
+              const bool slot_ok = IDX_IN_RANGE(
+                  slot_idx >= 0 && slot_idx < hdr->n_row_slots && pre + wcnt <= (uint32_t)TOPK, hdr,
+                  344);
               uint64_t* dst = p.cand_keys + slot_idx * TOPK + pre;
-              for (uint32_t e = lane; e < wcnt; e += 32) dst[e] = wreg[e];
-              if (tg == 0) p.cand_cnt[slot_idx] = n;
+              for (uint32_t e = lane; slot_ok && e < wcnt; e += 32) dst[e] = wreg[e];
+              if (tg == 0 && slot_ok) p.cand_cnt[slot_idx] = n;
               bar_sync(bar_id, kEpiThreads);
             }
           }

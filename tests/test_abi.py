@@ -36,6 +36,14 @@ def test_library_exports_every_declared_symbol():
     assert set(declared_functions()) <= set(_lib.EXPORTS)
 
 
+def test_range_checked_build_exports_the_same_symbols():
+    # the -DIDX_DEBUG_BOUNDS variant that the GPU tests run on small cases
+    lib = _lib.load(_lib.build(debug_bounds=True))
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.idx_topk_fp4_prefill(*([None] * 9), 512, None, None, None) == 1
+
+
 def test_supported_k_and_status_strings():
     import fp4_sparse_attention_tma_gb300 as m
     assert m.idx_topk_supported_k() == (512, 1024)
