@@ -510,6 +510,7 @@ int run(const Call& c, cudaStream_t stream) {
   sp.num_pages = pp.num_pages;
   sp.topk = c.topk;
   sp.mode = c.path == Path::kFused ? kModeSelect : kModeDense;
+  sp.dyn = sz.num_req > 1 ? 1 : 0;  // units of several requests differ in length
   sp.score_thr = pp.score_thr;
   sp.hdr = pp.hdr;
   sp.blocks = pp.blocks;
@@ -701,6 +702,7 @@ int run_fixed_scratch(const Call& c, cudaStream_t stream) {
   sp.num_pages = pp.num_pages;
   sp.topk = c.topk;
   sp.mode = kModeSelect;
+  sp.dyn = sz.num_req > 1 ? 1 : 0;  // units of several requests differ in length
   sp.score_thr = pp.score_thr;
   sp.hdr = pp.hdr;
   sp.blocks = pp.blocks;
@@ -1028,6 +1030,7 @@ int run_shard(const Call& c, int32_t c0, int32_t c1, const idx_tensor_t* out_sco
   sp.num_pages = pp.num_pages;
   sp.topk = c.topk;
   sp.mode = kModeSelect;
+  sp.dyn = sz.num_req > 1 ? 1 : 0;  // units of several requests differ in length
   sp.score_thr = 0;
   sp.hdr = pp.hdr;
   sp.blocks = pp.blocks;
@@ -1245,6 +1248,7 @@ int run_stream_ordered(const Call& c, void* workspace, uint64_t workspace_bytes,
   sp.num_pages = pp.num_pages;
   sp.topk = c.topk;
   sp.mode = kModeSelect;
+  sp.dyn = sz.num_req > 1 ? 1 : 0;  // units of several requests differ in length
   sp.score_thr = pp.score_thr;
   sp.hdr = pp.hdr;
   sp.blocks = pp.blocks;

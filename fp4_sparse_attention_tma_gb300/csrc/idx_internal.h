@@ -80,7 +80,8 @@ struct PlanHeader {
   int32_t unit_tiles;   // chunk length the planner chose
   int64_t n_row_slots;  // candidate row-slots in use
   uint32_t err_site;    // where the first error was raised (diagnostics)
-  uint32_t pad[9];
+  uint32_t claim;       // next schedule position of the dynamically scheduled scorer
+  uint32_t pad[8];
 };
 
 // Byte offsets of the scratch regions of one call.
@@ -150,6 +151,8 @@ struct ScoreParams {
   const int32_t* row_end;
   int32_t rows, max_pages, num_pages, topk;
   int32_t mode, score_thr;
+  int32_t dyn;               // 1: the CTAs claim work units from hdr->claim (several requests)
+  int32_t pad1;
   PlanHeader* hdr;
   const BlockInfo* blocks;
   const UnitInfo* units;

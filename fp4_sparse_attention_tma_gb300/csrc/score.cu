@@ -70,7 +70,8 @@ static_assert(kOffSfaAtom % 128 == 0 && kOffSfbAtom % 128 == 0 && kOffCand % 16 
 // misc region
 constexpr uint32_t kMiscTmem = 0, kMiscAbort = 4, kMiscTau = 32,
                    kMiscBc = 64,    // [3 rows][8 words] selection scratch
-                   kMiscWc = 160;   // [3 rows][4 warps] region counts
+                   kMiscWc = 160,   // [3 rows][4 warps] region counts
+                   kMiscUnit = 224; // [2 q buffers] claimed schedule position (dynamic mode)
 
 // barriers (8 bytes each)
 constexpr int kBarFull = 0;                                  // [kStages]
@@ -120,11 +121,16 @@ __host__ __device__ constexpr size_t smem_bytes_for(int mode, int topk) {
 
 static_assert(smem_bytes_for(kModeSelect, 1024) <= kMaxSmem, "shared memory budget");
 
-// Bounded wait for the teardown: ignores the abort flag.
-__device__ void mbar_drain(uint32_t bar, uint32_t parity) {
+// Bounded wait for the teardown: ignores the abort flag.  A phase that does
+// not complete within 0.2 s means the barrier accounting went wrong (or an
+// earlier wait already failed): it is recorded as kErrTimeout, not passed over.
+__device__ void mbar_drain(uint32_t bar, uint32_t parity, PlanHeader* hdr, uint32_t site) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > 200000000ull) break;  // 0.2 s
+    if (global_timer_ns() - t0 > 200000000ull) {  // 0.2 s
+      raise_status(hdr, kErrTimeout, site);
+      break;
+    }
   }
 }
 
@@ -403,7 +409,12 @@ __device__ __forceinline__ UnitView load_unit(const ScoreParams& p, int ui) {
   return v;
 }
 
-template <int MODE, int TOPK>
+// DYN: the CTAs claim schedule positions from a global counter (longest unit
+// first) instead of taking the fixed deal of cta_unit; warp 0 claims and
+// publishes each position in shared memory before the unit's query block
+// arrives, and the other roles read it behind that barrier.  Chosen on the host
+// for calls with several requests, whose units differ in length.
+template <int MODE, int TOPK, bool DYN>
 __global__ void __launch_bounds__(kThreads, 1)
     score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
                  const ScoreParams p) {
@@ -449,6 +460,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto wait = [&](uint32_t b, uint32_t par, uint32_t site) -> bool {
     return mbar_wait(b, par, abort_flag, hdr, site);
   };
+  volatile int32_t* unit_slot = reinterpret_cast<volatile int32_t*>(smem + kOffMisc + kMiscUnit);
+  // dynamic mode: the schedule position of the CTA's unit i, published by warp
+  // 0 before the query buffer's barrier completes (-1: no unit is left)
+  auto claimed_unit = [&](int i) -> int {
+    const uint32_t qpar = (uint32_t)(i >> 1) & 1u;
+    if (!wait(bar(kBarQFull + (i & 1)), qpar, 330)) return -2;
+    return unit_slot[i & 1];
+  };
 
   if (warp == 0 || warp == kProducer2) {
     // ----------------------------------------------------- TMA producers ----
@@ -469,11 +488,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t q_issued[2] = {0, 0};
     bool ok = true;
     for (int i = 0; ok; ++i) {
-      const int ui = cta_unit(i);
-      if (ui >= n_units) break;
-      const UnitView uv = load_unit(p, ui);
       const int qb = i & 1;
       const uint32_t qpar = (uint32_t)(i >> 1) & 1u;
+      int ui;
+      if constexpr (DYN) {
+        if (pw == 0) {
+          // the query buffer is free again (units i - 2 done) before its
+          // position slot is rewritten
+          if (i >= 2) {
+            ok = wait(bar(kBarQEmpty + qb), qpar ^ 1u, 300) &&
+                 wait(bar(kBarEpiDone + qb), qpar ^ 1u, 301);
+            if (!ok) break;
+          }
+          int c = 0;
+          if (lane == 0) {
+            c = (int)atomicAdd(&hdr->claim, 1u);
+            if (c >= n_units) c = -1;
+            unit_slot[qb] = c;
+          }
+          ui = __shfl_sync(0xffffffffu, c, 0);
+          if (ui < 0) {
+            if (lane == 0) mbar_arrive(bar(kBarQFull + qb));  // releases the other roles
+            ++q_issued[qb];  // that arrival completed a phase of the buffer's barrier too
+            break;
+          }
+        } else {
+          ui = claimed_unit(i);
+          if (ui < 0) {
+            ok = ui == -1;
+            break;
+          }
+        }
+      } else {
+        ui = cta_unit(i);
+        if (ui >= n_units) break;
+      }
+      const UnitView uv = load_unit(p, ui);
       int32_t rs = 0, re = 0;
       bool act = false;
       if (lane < uv.b.nrows) {
@@ -483,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t act_mask = __ballot_sync(0xffffffffu, act);
       if (pw == 0) {
-        if (i >= 2) {
+        if (!DYN && i >= 2) {
           ok = wait(bar(kBarQEmpty + qb), qpar ^ 1u, 300) &&
                wait(bar(kBarEpiDone + qb), qpar ^ 1u, 301);
           if (!ok) break;
@@ -618,11 +668,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // wait for this warp's copies in flight (its stages have parity pw)
       for (uint32_t s2 = pw; s2 < (uint32_t)kStages; s2 += 2) {
         const uint32_t uses = n_issued > s2 ? (n_issued - s2 + kStages - 1) / kStages : 0;
-        if (uses) mbar_drain(bar(kBarFull + s2), (uses - 1u) & 1u);
+        if (uses) mbar_drain(bar(kBarFull + s2), (uses - 1u) & 1u, hdr, 305);
       }
       if (pw == 0)
         for (int b2 = 0; b2 < 2; ++b2)
-          if (q_issued[b2]) mbar_drain(bar(kBarQFull + b2), (q_issued[b2] - 1u) & 1u);
+          if (q_issued[b2]) mbar_drain(bar(kBarQFull + b2), (q_issued[b2] - 1u) & 1u, hdr, 306);
     }
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------ MMA issuers ----
@@ -637,12 +687,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t b_desc0 = desc_kmajor_sw64(sbase + kOffB);
     bool ok = true;
     for (int i = 0; ok; ++i) {
-      const int ui = cta_unit(i);
-      if (ui >= n_units) break;
-      const UnitInfo u = p.units[p.sched[ui]];
       const int qb = i & 1;
       const uint32_t qpar = (uint32_t)(i >> 1) & 1u;
-      if (!wait(bar(kBarQFull + qb), qpar, 310)) break;
+      int ui;
+      if constexpr (DYN) {
+        ui = claimed_unit(i);
+        if (ui < 0) break;
+      } else {
+        ui = cta_unit(i);
+        if (ui >= n_units) break;
+        if (!wait(bar(kBarQFull + qb), qpar, 310)) break;
+      }
+      const UnitInfo u = p.units[p.sched[ui]];
       // both issuers' copies from this atom buffer two units ago have completed
       if (i >= 2 && !wait(bar(kBarQEmpty + qb), qpar ^ 1u, 311)) break;
       const uint32_t atom_off = kOffSfbAtom + (2u * j + (uint32_t)qb) * kSfbAtomBytes;
@@ -696,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) {
       tc_commit(bar(kBarMmaFinal + j));
-      mbar_drain(bar(kBarMmaFinal + j), 0);
+      mbar_drain(bar(kBarMmaFinal + j), 0, hdr, 314);
     }
     __syncwarp();
   } else if (warp >= kEpiWarp0) {
@@ -714,11 +770,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_use = 0;
     bool ok = true;
     for (int i = 0; ok; ++i) {
-      const int ui = cta_unit(i);
-      if (ui >= n_units) break;
-      const UnitView uv = load_unit(p, ui);
       const int qb = i & 1;
       const uint32_t qpar = (uint32_t)(i >> 1) & 1u;
+      int ui;
+      if constexpr (DYN) {
+        ui = claimed_unit(i);
+        if (ui < 0) {
+          ok = ui == -1;
+          break;
+        }
+      } else {
+        ui = cta_unit(i);
+        if (ui >= n_units) break;
+      }
+      const UnitView uv = load_unit(p, ui);
       const bool valid = g < uv.b.nrows;
       const int64_t row = uv.b.row0 + g;
       const int32_t s0 = valid ? p.row_start[row] : 0;
@@ -743,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             p.cand_cnt[slot_idx] = 0;
         }
       } else {
-        if (!wait(bar(kBarQFull + qb), qpar, 320)) {
+        if (!DYN && !wait(bar(kBarQFull + qb), qpar, 320)) {
           ok = false;
         } else {
           uint64_t w2[32];  // the row's weights as packed pairs (heads 2p, 2p+1)
@@ -911,14 +976,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int MODE, int TOPK>
+template <int MODE, int TOPK, bool DYN>
 cudaError_t launch_score_t(const CUtensorMap& tk, const CUtensorMap& tq, const ScoreParams& p,
                            int grid, cudaStream_t stream) {
   const size_t smem = smem_bytes_for(MODE, TOPK);
   static std::atomic<bool> done[64] = {};
-  cudaError_t err = set_smem_once(score_kernel<MODE, TOPK>, (int)smem, done);
+  cudaError_t err = set_smem_once(score_kernel<MODE, TOPK, DYN>, (int)smem, done);
   if (err != cudaSuccess) return err;
-  score_kernel<MODE, TOPK><<<grid, kThreads, smem, stream>>>(tk, tq, p);
+  score_kernel<MODE, TOPK, DYN><<<grid, kThreads, smem, stream>>>(tk, tq, p);
   return cudaGetLastError();
 }
 
@@ -928,9 +993,14 @@ size_t score_smem_bytes(int mode, int topk) { return smem_bytes_for(mode, topk);
 
 cudaError_t launch_score(const CUtensorMap& tmap_k, const CUtensorMap& tmap_q, const ScoreParams& p,
                          int grid, cudaStream_t stream) {
-  if (p.mode == kModeDense) return launch_score_t<kModeDense, 0>(tmap_k, tmap_q, p, grid, stream);
-  if (p.topk == 512) return launch_score_t<kModeSelect, 512>(tmap_k, tmap_q, p, grid, stream);
-  if (p.topk == 1024) return launch_score_t<kModeSelect, 1024>(tmap_k, tmap_q, p, grid, stream);
+  if (p.mode == kModeDense)
+    return launch_score_t<kModeDense, 0, false>(tmap_k, tmap_q, p, grid, stream);
+  if (p.topk == 512)
+    return p.dyn ? launch_score_t<kModeSelect, 512, true>(tmap_k, tmap_q, p, grid, stream)
+                 : launch_score_t<kModeSelect, 512, false>(tmap_k, tmap_q, p, grid, stream);
+  if (p.topk == 1024)
+    return p.dyn ? launch_score_t<kModeSelect, 1024, true>(tmap_k, tmap_q, p, grid, stream)
+                 : launch_score_t<kModeSelect, 1024, false>(tmap_k, tmap_q, p, grid, stream);
   return cudaErrorInvalidValue;
 }
 
