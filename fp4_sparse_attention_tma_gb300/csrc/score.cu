@@ -850,8 +850,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < uv.b.nrows; ++j)
             n_act += (p.row_end[uv.b.row0 + j] - p.row_start[uv.b.row0 + j]) > p.score_thr;
           // A tile's score is reduced at the end of the tile; its select step
-          // runs one tile late, right after the next tile's first TMEM load is
-          // issued, so that its dependent chain overlaps that load.  The first
+          // runs one tile late, at the end of the next tile, after that tile's
+          // accumulator buffer has been released: nothing between the wait for
+          // a buffer and its release delays the next MMA into it.  The first
           // call of a unit is a no-op (pwin false).
           float psc = 0.f;
           int32_t pslot = 0;
@@ -893,7 +894,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             };
             tmem_ld16(tb, xa);
-            tail();  // previous tile
+            if constexpr (MODE == kModeDense) tail();  // (its registers fit better here)
             tmem_wait_ld16(xa);
             tmem_ld16(tb + 16u, xb);
             dump(xa, 0);
@@ -912,6 +913,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++acc_use;
             dump(xb, 48);
             head_sum_part<24>(xb, w2, acc);
+            if constexpr (MODE == kModeSelect) tail();  // previous tile
             psc = head_sum_final(acc);
             pslot = slot;
             pwin = in_win;
