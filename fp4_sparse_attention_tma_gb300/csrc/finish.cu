@@ -294,7 +294,8 @@ __device__ __forceinline__ void team_rows(const FinishParams& p, int64_t blk, Te
 struct FinSmem {
   uint64_t buf[kFinCap];
   uint32_t hist[256];
-  uint32_t uoff[kFinThreads];           // first buffer position of each unit's keys
+  uint32_t uoff[kFinThreads];           // keys of the row's units before each unit
+  uint32_t ucnt[kFinThreads];           // keys of each unit (at most TOPK)
   uint32_t wsum[kFinThreads / 32];
   uint32_t bc[4];
   uint32_t cnt;
@@ -389,8 +390,11 @@ __device__ __forceinline__ void finish_row(const FinishParams& p, int64_t r, Fin
   } else {
     const BlockInfo bi = p.blocks[p.row_block[r]];
     const int j = (int)(r - bi.row0);
-    // When the row's units hold at most kFinCap keys together, gather them all
-    // at once (unit u's keys to buf[uoff[u] ..]) instead of unit by unit.
+    // The row's units in groups of kGroup: each thread loads all its keys of a
+    // group before it stores any (one memory round trip per group instead of
+    // one per key), unit u's keys to consecutive slots after those of the
+    // group's earlier units.  Before a group that does not fit the buffer's
+    // free space the buffer is reduced to the TOPK largest keys.
     bool gathered = false;
     if (bi.n_units <= kFinThreads) {
       uint32_t c = 0;
@@ -414,24 +418,45 @@ __device__ __forceinline__ void finish_row(const FinishParams& p, int64_t r, Fin
         total += ws;
       }
       sm.uoff[tid] = before + x - c;
+      sm.ucnt[tid] = c;
       __syncthreads();
-      if (total <= (uint32_t)kFinCap) {  // the same decision in every thread
-        for (uint32_t i = tid; i < total; i += kFinThreads) {
-          // the last unit starting at or before i (units without keys share
-          // their successor's start and are skipped this way)
-          int lo = 0, hi = bi.n_units - 1;
-          while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (sm.uoff[mid] <= i) lo = mid;
-            else hi = mid - 1;
-          }
-          const int64_t slot = bi.slot0 + (int64_t)lo * bi.nrows + j;
-          buf[i] = p.cand_keys[slot * TOPK + (i - sm.uoff[lo])];
+      constexpr int kE = TOPK / kFinThreads;        // keys of one unit per thread
+      constexpr int kGroup = (kFinCap - TOPK) / TOPK;  // fits after a reduction to TOPK
+      static_assert(kGroup >= 1, "buffer capacity");
+      for (int u0 = 0; u0 < bi.n_units; u0 += kGroup) {
+        const int u1 = min(u0 + kGroup, bi.n_units);
+        const uint32_t gsize = (u1 < bi.n_units ? sm.uoff[u1] : total) - sm.uoff[u0];
+        uint32_t base = *(volatile uint32_t*)&cnt;
+        if (base + gsize > (uint32_t)kFinCap) {  // the same decision in every thread
+          sel_compact<kFinThreads, kFinCap>(buf, &cnt, &tau, hist, bc, TOPK, tid, kFinBar, p.hdr);
+          base = *(volatile uint32_t*)&cnt;
         }
-        if (tid == 0) cnt = total;
-        gathered = true;
+        uint64_t v[kGroup * kE];
+#pragma unroll
+        for (int q = 0; q < kGroup * kE; ++q) {
+          const int u = u0 + q / kE;
+          const uint32_t i = (uint32_t)(tid + (q % kE) * kFinThreads);
+          const bool in = u < u1 && i < sm.ucnt[u];
+          v[q] = in ? p.cand_keys[(bi.slot0 + (int64_t)u * bi.nrows + j) * TOPK + i] : 0ull;
+        }
+#pragma unroll
+        for (int q = 0; q < kGroup * kE; ++q) {
+          const int u = u0 + q / kE;
+          const uint32_t i = (uint32_t)(tid + (q % kE) * kFinThreads);
+          if (u < u1 && i < sm.ucnt[u]) {
+            const uint32_t pos = base + (sm.uoff[u] - sm.uoff[u0]) + i;
+            if (IDX_IN_RANGE(pos < (uint32_t)kFinCap, p.hdr, 433)) buf[pos] = v[q];
+          }
+        }
+        __syncthreads();
+        if (tid == 0) cnt = base + gsize;
+        __syncthreads();
       }
+      gathered = true;
     }
+    // a row of more than kFinThreads units (a window of over two million
+    // positions even at the smallest unit size): unit by unit through the
+    // selector
     for (int k = 0; !gathered && k < bi.n_units; ++k) {
       const int64_t slot = bi.slot0 + (int64_t)k * bi.nrows + j;
       if (!IDX_IN_RANGE(slot < p.hdr->n_row_slots, p.hdr, 432)) break;

@@ -269,8 +269,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   }
 }
 
-// One warp per row block: every page-table entry that some row's window
-// [start, end) touches must name a page in [0, num_pages).
+// One warp per row block: every page-table entry that the window [start, end)
+// of a row the scorer does not score (end - start <= score_thr) touches must
+// name a page in [0, num_pages).  The finishing step maps such a row's
+// positions through the page table.  The entries under a scored row's window
+// are checked by the scorer's producer warps, which read each of them before
+// the page's copy and raise the same error for an entry outside the range.
 __global__ void __launch_bounds__(256) validate_pages_kernel(PlanParams p) {
   PlanHeader* hdr = p.hdr;
   if (read_status(hdr) != kOk) return;
@@ -288,6 +292,7 @@ __global__ void __launch_bounds__(256) validate_pages_kernel(PlanParams p) {
       if (j < bi.nrows) {
         s[j] = p.row_start[bi.row0 + j];
         e[j] = p.row_end[bi.row0 + j];
+        if (e[j] - s[j] > p.score_thr) e[j] = s[j];  // scored: the scorer checks its pages
         if (e[j] > s[j]) {
           lo = min(lo, s[j]);
           hi = max(hi, e[j]);

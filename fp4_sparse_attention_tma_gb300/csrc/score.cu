@@ -649,6 +649,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = bar(kBarFull + st);
           const bool v0 = need0 && pg0 >= 0 && pg0 < p.num_pages;
           const bool v1 = need1 && pg1 >= 0 && pg1 < p.num_pages;
+          // this is the page-table check of the scored rows' windows (the
+          // planner's page check covers only the rows that are not scored)
           if ((need0 && !v0) || (need1 && !v1)) raise_status(hdr, kErrInvalidPage, 303);
           const uint32_t bytes = ((uint32_t)v0 + (uint32_t)v1) * kPageBytes;
           if (bytes) {
