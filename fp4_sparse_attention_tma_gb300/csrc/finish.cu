@@ -525,6 +525,27 @@ union FinishShared {
   FinSmem merge;
 };
 
+// The CTA that finishes last (every CTA's writes are fenced before it counts
+// itself on the header) publishes the call's status and, on an error, fills
+// the outputs with -1.
+__device__ __forceinline__ void publish_if_last(const FinishParams& p) {
+  __shared__ uint32_t s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(&p.hdr->fin_done, 1u) == gridDim.x - 1u;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const uint32_t st = read_status(p.hdr);
+  if (threadIdx.x == 0) *p.status_out = st;
+  if (st == kOk) return;
+  const int64_t n = (int64_t)p.rows * p.topk;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+    if (p.out_phys) p.out_phys[i] = -1;
+    if (p.out_raw) p.out_raw[i] = -1;
+  }
+}
+
 template <int TOPK, bool SCORES>
 __global__ void __launch_bounds__(kFinThreads) finish_fused_kernel(FinishParams p, int team_blocks) {
   static_assert(kTeamThreads == kFinThreads, "one block shape for both paths");
@@ -535,6 +556,7 @@ __global__ void __launch_bounds__(kFinThreads) finish_fused_kernel(FinishParams 
     merge_rows<TOPK, kSrcUnits, SCORES>(p, (int64_t)blockIdx.x - team_blocks,
                                         (int64_t)gridDim.x - team_blocks, sh.merge);
   }
+  if (p.status_out) publish_if_last(p);
 }
 
 // Row windows: 0 <= start <= end <= width, and (row_req non-null) a request
@@ -689,28 +711,6 @@ cudaError_t launch_tile_merge(const TileMergeParams& p, cudaStream_t stream) {
   if (p.topk == 512) tile_merge_kernel<512><<<p.rows, kFinThreads, 0, stream>>>(p);
   else if (p.topk == 1024) tile_merge_kernel<1024><<<p.rows, kFinThreads, 0, stream>>>(p);
   else return cudaErrorInvalidValue;
-  return cudaGetLastError();
-}
-
-namespace {
-__global__ void publish_status_kernel(const PlanHeader* hdr, uint32_t* status_out,
-                                      int32_t* out_phys, int32_t* out_raw, int64_t n) {
-  const uint32_t st = read_status(hdr);
-  if (blockIdx.x == 0 && threadIdx.x == 0) *status_out = st;
-  if (st == kOk) return;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    out_phys[i] = -1;
-    if (out_raw) out_raw[i] = -1;
-  }
-}
-}  // namespace
-
-cudaError_t launch_publish_status(const PlanHeader* hdr, uint32_t* status_out, int32_t* out_phys,
-                                  int32_t* out_raw, int64_t n, cudaStream_t stream) {
-  const int64_t want = (n + 255) / 256;
-  const int grid = (int)(want < 1 ? 1 : (want > 1024 ? 1024 : want));
-  publish_status_kernel<<<grid, 256, 0, stream>>>(hdr, status_out, out_phys, out_raw, n);
   return cudaGetLastError();
 }
 

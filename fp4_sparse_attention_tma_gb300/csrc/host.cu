@@ -459,7 +459,6 @@ int run(const Call& c, cudaStream_t stream) {
     cudaGetLastError();
     return fail(IDX_ERR_CUDA);
   }
-  cudaMemsetAsync(s.hdr(), 0, sizeof(PlanHeader), stream);
   float* score_buf = nullptr;
   if (c.path != Path::kFused)
     score_buf = c.scores ? (float*)c.scores->data : s.at<float>(ws_off);
@@ -476,6 +475,7 @@ int run(const Call& c, cudaStream_t stream) {
   pp.score_thr = c.path == Path::kDebug ? 0 : c.topk;
   pp.grid = grid;
   pp.check_end_le = c.path == Path::kFused ? -1 : (int32_t)check_end;
+  pp.clear_hdr = 1;
   pp.max_units = s.L.max_units;
   pp.max_row_slots = s.L.max_row_slots;
   pp.hdr = s.hdr();
@@ -655,10 +655,6 @@ int run_fixed_scratch(const Call& c, cudaStream_t stream) {
   s.L = scratch_layout(sz.rows, c.topk, grid, true);
   if (s.L.total > (size_t)IDX_NOALLOC_SCRATCH_BYTES) return fail(IDX_ERR_SCRATCH_LIMIT);
   if ((st = fixed_scratch(dev, &s.base))) return fail(st);
-  if (cudaMemsetAsync(s.hdr(), 0, sizeof(PlanHeader), stream) != cudaSuccess) {
-    cudaGetLastError();
-    return fail(IDX_ERR_CUDA);
-  }
 
   PlanParams pp{};
   pp.row_req = (const int32_t*)c.row_req->data;
@@ -672,6 +668,7 @@ int run_fixed_scratch(const Call& c, cudaStream_t stream) {
   pp.score_thr = c.topk;
   pp.grid = grid;
   pp.check_end_le = -1;
+  pp.clear_hdr = 1;
   pp.max_units = s.L.max_units;
   pp.max_row_slots = s.L.max_row_slots;
   pp.hdr = s.hdr();
@@ -1207,7 +1204,7 @@ int run_stream_ordered(const Call& c, void* workspace, uint64_t workspace_bytes,
                                                                                    : IDX_ERR_CUDA;
   }
   s.base = workspace;
-  int cuda_err = cudaMemsetAsync(s.hdr(), 0, sizeof(PlanHeader), stream) != cudaSuccess;
+  int cuda_err = 0;
 
   PlanParams pp{};
   pp.row_req = (const int32_t*)c.row_req->data;
@@ -1221,6 +1218,7 @@ int run_stream_ordered(const Call& c, void* workspace, uint64_t workspace_bytes,
   pp.score_thr = c.topk;
   pp.grid = grid;
   pp.check_end_le = -1;
+  pp.clear_hdr = 1;
   pp.max_units = s.L.max_units;
   pp.max_row_slots = s.L.max_row_slots;
   pp.hdr = s.hdr();
@@ -1273,9 +1271,8 @@ int run_stream_ordered(const Call& c, void* workspace, uint64_t workspace_bytes,
   fp.cand_keys = sp.cand_keys;
   fp.out_phys = (int32_t*)c.out_phys->data;
   fp.out_raw = c.out_raw ? (int32_t*)c.out_raw->data : nullptr;
+  fp.status_out = status_out;  // published by the finishing kernel's last CTA
   cuda_err |= launch_finish(fp, stream) != cudaSuccess;
-  cuda_err |= launch_publish_status(pp.hdr, status_out, fp.out_phys, fp.out_raw,
-                                    sz.rows * (int64_t)c.topk, stream) != cudaSuccess;
   if (cuda_err) {
     cudaGetLastError();
     return IDX_ERR_CUDA;

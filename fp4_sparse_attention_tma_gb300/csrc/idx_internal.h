@@ -81,7 +81,8 @@ struct PlanHeader {
   int64_t n_row_slots;  // candidate row-slots in use
   uint32_t err_site;    // where the first error was raised (diagnostics)
   uint32_t claim;       // next schedule position of the dynamically scheduled scorer
-  uint32_t pad[8];
+  uint32_t fin_done;    // CTAs of the finishing kernel that are done (status publishing)
+  uint32_t pad[7];
 };
 
 // Byte offsets of the scratch regions of one call.
@@ -126,7 +127,8 @@ struct PlanParams {
   int32_t score_thr;     // rows with end - start > score_thr are scored
   int32_t grid;          // persistent CTAs of the scorer
   int32_t check_end_le;  // >= 0: every end must be <= this (score matrix width); -1: none
-  int32_t pad;
+  int32_t clear_hdr;     // 1: the planner zeroes the header first (no kernel of the call
+                         // touches it before the planner); 0: the caller cleared it
   int64_t max_units, max_row_slots;
   PlanHeader* hdr;
   int32_t* row_block;    // row -> block
@@ -209,6 +211,9 @@ struct FinishParams {
   int32_t pad2;
   const float* shard_score;   // [n_shards, rows, topk]
   const int32_t* shard_raw;   // [n_shards, rows, topk], -1 = empty entry
+  // stream-ordered call (non-null): the finishing kernel's last CTA copies the
+  // call's status here and, on an error, fills out_phys / out_raw with -1
+  uint32_t* status_out;
 };
 
 }  // namespace idxk

@@ -61,10 +61,4 @@ cudaError_t launch_clip_windows(const int32_t* row_start, const int32_t* row_end
                                 int32_t* out_end, cudaStream_t stream);
 cudaError_t launch_tile_merge(const TileMergeParams& p, cudaStream_t stream);
 
-// Stream-ordered end of a call whose status is not read by the host: copies
-// the status word to `status_out` and, when it is not kOk, fills the n
-// entries of out_phys (and out_raw, when given) with -1.
-cudaError_t launch_publish_status(const PlanHeader* hdr, uint32_t* status_out, int32_t* out_phys,
-                                  int32_t* out_raw, int64_t n, cudaStream_t stream);
-
 }  // namespace idxk

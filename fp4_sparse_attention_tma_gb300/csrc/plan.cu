@@ -59,6 +59,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   extern __shared__ __align__(16) uint64_t s_sort[];
   const int tid = threadIdx.x;
   PlanHeader* hdr = p.hdr;
+  if (p.clear_hdr) {
+    // the call's first kernel starts from an empty header (status kOk, no
+    // claims); saves a separate clear on the stream
+    if (tid == 0) *hdr = PlanHeader{};
+    __syncthreads();
+  }
 
   // 1. row metadata
   for (int r = tid; r < p.rows; r += kPlanThreads) {
@@ -79,33 +85,42 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   __syncthreads();
   for (int64_t base = 0; base < p.rows; base += (int64_t)kPlanThreads * kRowsPerThread) {
     const int64_t r0 = base + (int64_t)tid * kRowsPerThread;
+    // the thread's rows' requests, loaded once: rq[k + 1] is row r0 + k's, rq[0]
+    // the previous row's (-1 before row 0 and past the last row)
+    int32_t rq[kRowsPerThread + 1];
+    rq[0] = (r0 > 0 && r0 <= p.rows) ? p.row_req[r0 - 1] : -1;
+#pragma unroll
+    for (int k = 0; k < kRowsPerThread; ++k) rq[k + 1] = r0 + k < p.rows ? p.row_req[r0 + k] : -1;
     int32_t last_seg = -1;
+#pragma unroll
     for (int k = 0; k < kRowsPerThread; ++k) {
       int64_t r = r0 + k;
-      if (r < p.rows && (r == 0 || p.row_req[r] != p.row_req[r - 1])) last_seg = (int32_t)r;
+      if (r < p.rows && (r == 0 || rq[k + 1] != rq[k])) last_seg = (int32_t)r;
     }
     int32_t incl = block_scan_incl<int32_t>(last_seg, s_tot32, MaxI32(), -1);
     int32_t excl = __shfl_up_sync(0xffffffffu, incl, 1);
     if ((tid & 31) == 0) excl = (tid >> 5) > 0 ? s_tot32[(tid >> 5) - 1] : -1;
     int32_t seg = excl >= 0 ? excl : s_carry_seg;
     int64_t nstart = 0;
+#pragma unroll
     for (int k = 0; k < kRowsPerThread; ++k) {
       int64_t r = r0 + k;
       if (r >= p.rows) break;
-      if (r == 0 || p.row_req[r] != p.row_req[r - 1]) seg = (int32_t)r;
-      if (((r - seg) % kRowsPerBlock) == 0) ++nstart;
+      if (r == 0 || rq[k + 1] != rq[k]) seg = (int32_t)r;
+      if (((int32_t)r - seg) % kRowsPerBlock == 0) ++nstart;
     }
     int64_t bincl = block_scan_incl<int64_t>(nstart, s_tot64, AddI64(), 0);
     int64_t b = s_carry_blocks + bincl - nstart;
     seg = excl >= 0 ? excl : s_carry_seg;
+#pragma unroll
     for (int k = 0; k < kRowsPerThread; ++k) {
       int64_t r = r0 + k;
       if (r >= p.rows) break;
-      if (r == 0 || p.row_req[r] != p.row_req[r - 1]) seg = (int32_t)r;
-      if (((r - seg) % kRowsPerBlock) == 0) {
+      if (r == 0 || rq[k + 1] != rq[k]) seg = (int32_t)r;
+      if (((int32_t)r - seg) % kRowsPerBlock == 0) {
         BlockInfo bi{};
         bi.row0 = (int32_t)r;
-        bi.req = p.row_req[r];
+        bi.req = rq[k + 1];
         p.blocks[b] = bi;
         ++b;
       }
@@ -158,6 +173,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   int64_t target = (int64_t)kUnitsPerCta * p.grid;
   int64_t unit_tiles = (tot_tiles + target - 1) / target;
   if (unit_tiles < kMinUnitTiles) unit_tiles = kMinUnitTiles;
+  // a block has fewer than 2^31 tiles: 32-bit arithmetic from here on
+  const int32_t ut = unit_tiles > INT32_MAX ? INT32_MAX : (int32_t)unit_tiles;
 
   // 4. units per block and candidate row-slots (blocks handled in tiles of
   //    kPlanThreads with a running carry)
@@ -176,7 +193,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     BlockInfo bi{};
     if (b < n_blocks) {
       bi = p.blocks[b];
-      nu = bi.ntiles > 0 ? (bi.ntiles + unit_tiles - 1) / unit_tiles : 0;
+      nu = bi.ntiles > 0 ? bi.ntiles / ut + (bi.ntiles % ut != 0) : 0;
       ns = nu * bi.nrows;
     }
     int64_t u_incl = block_scan_incl<int64_t>(nu, s_tot64, AddI64(), 0);
@@ -192,15 +209,26 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
         bi.slot0 = s_first;
         p.blocks[b] = bi;
         int32_t lmin = INT32_MAX, lmax = 0;
-        for (int64_t k = 0; k < nu; ++k) {
+        // unit k covers tiles tile0 + floor(k * ntiles / nu) .. of the next
+        // unit: with ntiles = q * nu + rr that is k * q + floor(k * rr / nu),
+        // whose second term grows by 0 or 1 per unit (the remainder k * rr mod
+        // nu is carried along, no division per unit)
+        const int32_t nu32 = (int32_t)nu;
+        const int32_t q = nu32 > 0 ? bi.ntiles / nu32 : 0, rr = nu32 > 0 ? bi.ntiles % nu32 : 0;
+        int32_t t_beg = bi.tile0, rem = 0;
+        for (int32_t k = 0; k < nu32; ++k) {
+          rem += rr;
+          const int32_t step = q + (rem >= nu32 ? 1 : 0);
+          if (rem >= nu32) rem -= nu32;
           UnitInfo u;
           u.block = (int32_t)b;
-          u.k = (int32_t)k;
-          u.t_begin = bi.tile0 + (int32_t)((k * bi.ntiles) / nu);
-          u.t_end = bi.tile0 + (int32_t)(((k + 1) * bi.ntiles) / nu);
+          u.k = k;
+          u.t_begin = t_beg;
+          u.t_end = t_beg + step;
+          t_beg = u.t_end;
           p.units[u_first + k] = u;
-          lmin = min(lmin, u.t_end - u.t_begin);
-          lmax = max(lmax, u.t_end - u.t_begin);
+          lmin = min(lmin, step);
+          lmax = max(lmax, step);
         }
         if (nu > 0) {
           atomicMin(&s_len_min, lmin);
