@@ -16,6 +16,7 @@ K cache, score = sum_h w * ReLU(q_h . k), and return the exact TopK positions
 from __future__ import annotations
 
 import ctypes
+import struct
 
 from . import _lib
 
@@ -50,7 +51,7 @@ def _desc(t):
         return None
     d = _lib.IdxTensor()
     d.data = t.data_ptr() if t.numel() > 0 else None
-    d.dtype = _DT.get(str(t.dtype).replace("torch.", ""), 0)
+    d.dtype = _dtype_code(t.dtype)
     d.ndim = t.dim()
     for i in range(min(4, t.dim())):
         d.shape[i] = t.shape[i]
@@ -58,8 +59,39 @@ def _desc(t):
     return d
 
 
-def _ref(d):
-    return ctypes.byref(d) if d is not None else None
+# idx_tensor_t as packed bytes: data pointer, dtype, ndim, shape[4], stride[4]
+_DESC = struct.Struct("=Qii4q4q")
+_ZERO4 = (0, 0, 0, 0)
+_DT_CODE = {}  # torch.dtype -> code, filled on first use
+
+
+def _dtype_code(dt) -> int:
+    c = _DT_CODE.get(dt)
+    if c is None:
+        c = _DT_CODE[dt] = _DT.get(str(dt).replace("torch.", ""), 0)
+    return c
+
+
+def _descs(ts):
+    """Descriptors of the tensors `ts` (None: absent) packed into one buffer.
+    Returns the buffer, which must stay alive for the call, and each
+    descriptor's address (None for an absent tensor)."""
+    buf = ctypes.create_string_buffer(_DESC.size * len(ts))
+    base = ctypes.addressof(buf)
+    addrs = [None] * len(ts)
+    for i, t in enumerate(ts):
+        if t is None:
+            continue
+        sh = t.shape
+        st = t.stride()
+        n = len(sh)
+        if n < 4:
+            sh = (*sh, *_ZERO4[n:])
+            st = (*st, *_ZERO4[n:])
+        _DESC.pack_into(buf, _DESC.size * i, t.data_ptr() if t.numel() else 0,
+                        _dtype_code(t.dtype), n, *sh[:4], *st[:4])
+        addrs[i] = base + _DESC.size * i
+    return buf, addrs
 
 
 def _stream(stream):
@@ -80,10 +112,10 @@ def idx_topk_fp4_prefill(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_tab
                          raise_on_error=True) -> int:
     """Fused scoring + exact TopK + page mapping; writes the outputs in place."""
     lib = _lib.load()
-    ds = [_desc(t) for t in (q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
-                             row_start, row_end, out_phys_slot, out_raw_idx)]
-    code = lib.idx_topk_fp4_prefill(*[_ref(d) for d in ds[:9]], int(topk), _ref(ds[9]),
-                                    _ref(ds[10]), _stream(stream))
+    keep, ds = _descs((q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                        row_start, row_end, out_phys_slot, out_raw_idx))
+    code = lib.idx_topk_fp4_prefill(*ds[:9], int(topk), ds[9],
+                                    ds[10], _stream(stream))
     return _check(code, "idx_topk_fp4_prefill", raise_on_error)
 
 
@@ -95,12 +127,12 @@ def idx_topk_fp4_prefill_host(q_fp4, q_scale, k_cache_fp4, k_scale, weights, pag
     outputs in place before returning."""
     import torch
     lib = _lib.load()
-    ds = [_desc(t) for t in (q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
-                             row_start, row_end, out_phys_slot, out_raw_idx)]
+    keep, ds = _descs((q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                        row_start, row_end, out_phys_slot, out_raw_idx))
     if stream is None:
         stream = torch.cuda.current_stream(int(device))
-    code = lib.idx_topk_fp4_prefill_host(*[_ref(d) for d in ds[:9]], int(topk), _ref(ds[9]),
-                                         _ref(ds[10]), int(device), _stream(stream))
+    code = lib.idx_topk_fp4_prefill_host(*ds[:9], int(topk), ds[9],
+                                         ds[10], int(device), _stream(stream))
     return _check(code, "idx_topk_fp4_prefill_host", raise_on_error)
 
 
@@ -110,10 +142,10 @@ def idx_topk_fp4_prefill_paged(q_fp4, q_scale, k_pages, weights, page_table, row
     """idx_topk_fp4_prefill on a page-interleaved K cache u8 [NP, 4352]
     (each page: 4096 code bytes, then 256 scale bytes)."""
     lib = _lib.load()
-    ds = [_desc(t) for t in (q_fp4, q_scale, k_pages, weights, page_table, row_req, row_start,
-                             row_end, out_phys_slot, out_raw_idx)]
-    code = lib.idx_topk_fp4_prefill_paged(*[_ref(d) for d in ds[:8]], int(topk), _ref(ds[8]),
-                                          _ref(ds[9]), _stream(stream))
+    keep, ds = _descs((q_fp4, q_scale, k_pages, weights, page_table, row_req, row_start,
+                        row_end, out_phys_slot, out_raw_idx))
+    code = lib.idx_topk_fp4_prefill_paged(*ds[:8], int(topk), ds[8],
+                                          ds[9], _stream(stream))
     return _check(code, "idx_topk_fp4_prefill_paged", raise_on_error)
 
 
@@ -125,10 +157,10 @@ def idx_topk_fp4_prefill_async(q_fp4, q_scale, k_cache_fp4, k_scale, weights, pa
     bytes; `status` an int32 device tensor of one element that receives the
     device-side status."""
     lib = _lib.load()
-    ds = [_desc(t) for t in (q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
-                             row_start, row_end, out_phys_slot, out_raw_idx)]
-    code = lib.idx_topk_fp4_prefill_async(*[_ref(d) for d in ds[:9]], int(topk), _ref(ds[9]),
-                                          _ref(ds[10]), ctypes.c_void_p(workspace.data_ptr()),
+    keep, ds = _descs((q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                        row_start, row_end, out_phys_slot, out_raw_idx))
+    code = lib.idx_topk_fp4_prefill_async(*ds[:9], int(topk), ds[9],
+                                          ds[10], ctypes.c_void_p(workspace.data_ptr()),
                                           ctypes.c_uint64(workspace.numel() * workspace.element_size()),
                                           ctypes.c_void_p(status.data_ptr()), _stream(stream))
     return _check(code, "idx_topk_fp4_prefill_async", raise_on_error)
@@ -142,10 +174,10 @@ def idx_topk_fp4_prefill_noalloc(q_fp4, q_scale, k_cache_fp4, k_scale, weights, 
     a per-device lock held until the call's work has completed, so they never
     overlap on the buffer; the call returns after its stream has finished."""
     lib = _lib.load()
-    ds = [_desc(t) for t in (q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
-                             row_start, row_end, out_phys_slot, out_raw_idx)]
-    code = lib.idx_topk_fp4_prefill_noalloc(*[_ref(d) for d in ds[:9]], int(topk), _ref(ds[9]),
-                                            _ref(ds[10]), _stream(stream))
+    keep, ds = _descs((q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                        row_start, row_end, out_phys_slot, out_raw_idx))
+    code = lib.idx_topk_fp4_prefill_noalloc(*ds[:9], int(topk), ds[9],
+                                            ds[10], _stream(stream))
     return _check(code, "idx_topk_fp4_prefill_noalloc", raise_on_error)
 
 
@@ -155,10 +187,10 @@ def idx_topk_fp4_prefill_mma_scales(q_fp4, q_scale, k_cache_fp4, k_scale_mma, we
     """idx_topk_fp4_prefill with the K scales [NP, 256] in the MMA's
     scale-copy order: byte 8j + 4h + b of a page = scale b of slot 32h + j."""
     lib = _lib.load()
-    ds = [_desc(t) for t in (q_fp4, q_scale, k_cache_fp4, k_scale_mma, weights, page_table,
-                             row_req, row_start, row_end, out_phys_slot, out_raw_idx)]
-    code = lib.idx_topk_fp4_prefill_mma_scales(*[_ref(d) for d in ds[:9]], int(topk),
-                                               _ref(ds[9]), _ref(ds[10]), _stream(stream))
+    keep, ds = _descs((q_fp4, q_scale, k_cache_fp4, k_scale_mma, weights, page_table,
+                        row_req, row_start, row_end, out_phys_slot, out_raw_idx))
+    code = lib.idx_topk_fp4_prefill_mma_scales(*ds[:9], int(topk),
+                                               ds[9], ds[10], _stream(stream))
     return _check(code, "idx_topk_fp4_prefill_mma_scales", raise_on_error)
 
 
@@ -169,10 +201,10 @@ def idx_topk_fp4_prefill_shard(q_fp4, q_scale, k_cache_fp4, k_scale, weights, pa
     its window inside [ctx_begin, ctx_end); writes that part's exact TopK
     (scores f32 and positions i32 [R, topk], -1 / NaN padded) in place."""
     lib = _lib.load()
-    ds = [_desc(t) for t in (q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
-                             row_start, row_end, out_score, out_raw_idx)]
-    code = lib.idx_topk_fp4_prefill_shard(*[_ref(d) for d in ds[:9]], int(ctx_begin),
-                                          int(ctx_end), int(topk), _ref(ds[9]), _ref(ds[10]),
+    keep, ds = _descs((q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                        row_start, row_end, out_score, out_raw_idx))
+    code = lib.idx_topk_fp4_prefill_shard(*ds[:9], int(ctx_begin),
+                                          int(ctx_end), int(topk), ds[9], ds[10],
                                           _stream(stream))
     return _check(code, "idx_topk_fp4_prefill_shard", raise_on_error)
 
@@ -183,10 +215,10 @@ def idx_topk_merge_shards(shard_score, shard_raw, page_table, row_req, row_start
     """Exact merge of S context-shard lists [S, R, topk] into the TopK outputs
     (short-row contract and page mapping included)."""
     lib = _lib.load()
-    ds = [_desc(t) for t in (shard_score, shard_raw, page_table, row_req, row_start, row_end,
-                             out_phys_slot, out_raw_idx)]
-    code = lib.idx_topk_merge_shards(*[_ref(d) for d in ds[:6]], int(topk), _ref(ds[6]),
-                                     _ref(ds[7]), _stream(stream))
+    keep, ds = _descs((shard_score, shard_raw, page_table, row_req, row_start, row_end,
+                        out_phys_slot, out_raw_idx))
+    code = lib.idx_topk_merge_shards(*ds[:6], int(topk), ds[6],
+                                     ds[7], _stream(stream))
     return _check(code, "idx_topk_merge_shards", raise_on_error)
 
 
@@ -195,10 +227,10 @@ def idx_dense_topk_fp4_prefill(q_fp4, q_scale, k_cache_fp4, k_scale, weights, pa
                                score_workspace=None, stream=None, raise_on_error=True) -> int:
     """Comparison path: materialised fp32 scores, then a separate TopK."""
     lib = _lib.load()
-    ds = [_desc(t) for t in (q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
-                             row_start, row_end, out_phys_slot, out_raw_idx, score_workspace)]
-    code = lib.idx_dense_topk_fp4_prefill(*[_ref(d) for d in ds[:9]], int(topk), _ref(ds[9]),
-                                          _ref(ds[10]), _ref(ds[11]), _stream(stream))
+    keep, ds = _descs((q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                        row_start, row_end, out_phys_slot, out_raw_idx, score_workspace))
+    code = lib.idx_dense_topk_fp4_prefill(*ds[:9], int(topk), ds[9],
+                                          ds[10], ds[11], _stream(stream))
     return _check(code, "idx_dense_topk_fp4_prefill", raise_on_error)
 
 
@@ -208,10 +240,10 @@ def idx_tiled_topk_fp4_prefill(q_fp4, q_scale, k_cache_fp4, k_scale, weights, pa
     """Comparison path: score `context_tile` positions at a time into a bounded
     fp32 buffer, fold each chunk into the rows' running TopK."""
     lib = _lib.load()
-    ds = [_desc(t) for t in (q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
-                             row_start, row_end, out_phys_slot, out_raw_idx)]
-    code = lib.idx_tiled_topk_fp4_prefill(*[_ref(d) for d in ds[:9]], int(topk), int(context_tile),
-                                          _ref(ds[9]), _ref(ds[10]), _stream(stream))
+    keep, ds = _descs((q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                        row_start, row_end, out_phys_slot, out_raw_idx))
+    code = lib.idx_tiled_topk_fp4_prefill(*ds[:9], int(topk), int(context_tile),
+                                          ds[9], ds[10], _stream(stream))
     return _check(code, "idx_tiled_topk_fp4_prefill", raise_on_error)
 
 
@@ -220,9 +252,9 @@ def idx_fp4_debug_scores(q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_tab
                          raise_on_error=True) -> int:
     """Scores (and optionally per-head logits) from the same scoring kernel."""
     lib = _lib.load()
-    ds = [_desc(t) for t in (q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
-                             row_start, row_end, out_scores, out_logits)]
-    code = lib.idx_fp4_debug_scores(*[_ref(d) for d in ds], _stream(stream))
+    keep, ds = _descs((q_fp4, q_scale, k_cache_fp4, k_scale, weights, page_table, row_req,
+                        row_start, row_end, out_scores, out_logits))
+    code = lib.idx_fp4_debug_scores(*ds, _stream(stream))
     return _check(code, "idx_fp4_debug_scores", raise_on_error)
 
 
@@ -230,9 +262,9 @@ def idx_topk_select_scores(scores, row_start, row_end, topk, out_raw_idx, stream
                            raise_on_error=True) -> int:
     """Exact TopK of a materialised fp32 score matrix under the total order."""
     lib = _lib.load()
-    ds = [_desc(t) for t in (scores, row_start, row_end, out_raw_idx)]
-    code = lib.idx_topk_select_scores(_ref(ds[0]), _ref(ds[1]), _ref(ds[2]), int(topk),
-                                      _ref(ds[3]), _stream(stream))
+    keep, ds = _descs((scores, row_start, row_end, out_raw_idx))
+    code = lib.idx_topk_select_scores(ds[0], ds[1], ds[2], int(topk),
+                                      ds[3], _stream(stream))
     return _check(code, "idx_topk_select_scores", raise_on_error)
 
 

@@ -86,42 +86,45 @@ class IdxTensor(ctypes.Structure):
                 ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
 
 
+# descriptors are passed as addresses (the binding packs them into one buffer per call)
+_DESC_PTR = ctypes.c_void_p
+
 EXPORTS = {
-    "idx_topk_fp4_prefill": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
-                             [ctypes.c_int32, ctypes.POINTER(IdxTensor), ctypes.POINTER(IdxTensor),
+    "idx_topk_fp4_prefill": (ctypes.c_int, [_DESC_PTR] * 9 +
+                             [ctypes.c_int32, _DESC_PTR, _DESC_PTR,
                               ctypes.c_void_p]),
-    "idx_topk_fp4_prefill_paged": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 8 +
-                                   [ctypes.c_int32, ctypes.POINTER(IdxTensor),
-                                    ctypes.POINTER(IdxTensor), ctypes.c_void_p]),
-    "idx_topk_fp4_prefill_async": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
-                                   [ctypes.c_int32, ctypes.POINTER(IdxTensor),
-                                    ctypes.POINTER(IdxTensor), ctypes.c_void_p, ctypes.c_uint64,
+    "idx_topk_fp4_prefill_paged": (ctypes.c_int, [_DESC_PTR] * 8 +
+                                   [ctypes.c_int32, _DESC_PTR,
+                                    _DESC_PTR, ctypes.c_void_p]),
+    "idx_topk_fp4_prefill_async": (ctypes.c_int, [_DESC_PTR] * 9 +
+                                   [ctypes.c_int32, _DESC_PTR,
+                                    _DESC_PTR, ctypes.c_void_p, ctypes.c_uint64,
                                     ctypes.c_void_p, ctypes.c_void_p]),
-    "idx_topk_fp4_prefill_host": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
-                                  [ctypes.c_int32, ctypes.POINTER(IdxTensor),
-                                   ctypes.POINTER(IdxTensor), ctypes.c_int32, ctypes.c_void_p]),
-    "idx_topk_fp4_prefill_noalloc": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
-                                     [ctypes.c_int32, ctypes.POINTER(IdxTensor),
-                                      ctypes.POINTER(IdxTensor), ctypes.c_void_p]),
-    "idx_topk_fp4_prefill_mma_scales": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
-                                        [ctypes.c_int32, ctypes.POINTER(IdxTensor),
-                                         ctypes.POINTER(IdxTensor), ctypes.c_void_p]),
-    "idx_topk_fp4_prefill_shard": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
+    "idx_topk_fp4_prefill_host": (ctypes.c_int, [_DESC_PTR] * 9 +
+                                  [ctypes.c_int32, _DESC_PTR,
+                                   _DESC_PTR, ctypes.c_int32, ctypes.c_void_p]),
+    "idx_topk_fp4_prefill_noalloc": (ctypes.c_int, [_DESC_PTR] * 9 +
+                                     [ctypes.c_int32, _DESC_PTR,
+                                      _DESC_PTR, ctypes.c_void_p]),
+    "idx_topk_fp4_prefill_mma_scales": (ctypes.c_int, [_DESC_PTR] * 9 +
+                                        [ctypes.c_int32, _DESC_PTR,
+                                         _DESC_PTR, ctypes.c_void_p]),
+    "idx_topk_fp4_prefill_shard": (ctypes.c_int, [_DESC_PTR] * 9 +
                                    [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                    ctypes.POINTER(IdxTensor), ctypes.POINTER(IdxTensor),
+                                    _DESC_PTR, _DESC_PTR,
                                     ctypes.c_void_p]),
-    "idx_topk_merge_shards": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 6 +
-                              [ctypes.c_int32, ctypes.POINTER(IdxTensor),
-                               ctypes.POINTER(IdxTensor), ctypes.c_void_p]),
-    "idx_tiled_topk_fp4_prefill": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
-                                   [ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(IdxTensor),
-                                    ctypes.POINTER(IdxTensor), ctypes.c_void_p]),
-    "idx_dense_topk_fp4_prefill": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 9 +
-                                   [ctypes.c_int32] + [ctypes.POINTER(IdxTensor)] * 3 +
+    "idx_topk_merge_shards": (ctypes.c_int, [_DESC_PTR] * 6 +
+                              [ctypes.c_int32, _DESC_PTR,
+                               _DESC_PTR, ctypes.c_void_p]),
+    "idx_tiled_topk_fp4_prefill": (ctypes.c_int, [_DESC_PTR] * 9 +
+                                   [ctypes.c_int32, ctypes.c_int32, _DESC_PTR,
+                                    _DESC_PTR, ctypes.c_void_p]),
+    "idx_dense_topk_fp4_prefill": (ctypes.c_int, [_DESC_PTR] * 9 +
+                                   [ctypes.c_int32] + [_DESC_PTR] * 3 +
                                    [ctypes.c_void_p]),
-    "idx_fp4_debug_scores": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 11 + [ctypes.c_void_p]),
-    "idx_topk_select_scores": (ctypes.c_int, [ctypes.POINTER(IdxTensor)] * 3 +
-                               [ctypes.c_int32, ctypes.POINTER(IdxTensor), ctypes.c_void_p]),
+    "idx_fp4_debug_scores": (ctypes.c_int, [_DESC_PTR] * 11 + [ctypes.c_void_p]),
+    "idx_topk_select_scores": (ctypes.c_int, [_DESC_PTR] * 3 +
+                               [ctypes.c_int32, _DESC_PTR, ctypes.c_void_p]),
     "idx_topk_supported_k": (ctypes.c_int, [ctypes.POINTER(ctypes.POINTER(ctypes.c_int32)),
                                             ctypes.POINTER(ctypes.c_int32)]),
     "idx_topk_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -137,6 +140,8 @@ EXPORTS = {
 def load(path: str = None):
     """Build if needed, then open the library and declare its C ABI."""
     global _lib
+    if path is None and _lib is not None:
+        return _lib
     with _lock:
         if _lib is not None and path is None:
             return _lib

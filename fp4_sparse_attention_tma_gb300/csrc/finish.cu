@@ -25,11 +25,20 @@ constexpr int kFinBatch = kFinThreads * kFinPer;
 constexpr uint32_t kFinBar = 1;
 constexpr int kFinGridCap = 2048;  // merging CTAs (rows strided over them)
 
-__device__ __forceinline__ int32_t map_phys(const int32_t* row_pt, int32_t raw) {
+// Physical slot of position raw of a row (page table row_pt), -1 for raw < 0.
+// The entry must name a page in [0, num_pages); one that does not maps to -1
+// and sets `bad`, which the caller turns into kErrInvalidPage (the call fails
+// closed).  This is the page-table check of the rows the scorer does not score
+// (their every position is mapped here); the scorer's producers check the
+// entries under the scored rows' windows.  (The windows, hence raw / 64 <
+// max_pages, were validated by the plan.)
+__device__ __forceinline__ int32_t map_phys(const int32_t* row_pt, int32_t raw, int32_t num_pages,
+                                            bool& bad) {
   if (raw < 0 || row_pt == nullptr) return -1;
-  // (the windows, hence raw / 64 < max_pages, were validated by the plan)
-  const int64_t v = (int64_t)row_pt[raw >> 6] * kPage + (raw & (kPage - 1));
-  return (int32_t)v;
+  const int32_t pg = row_pt[raw >> 6];
+  const bool ok = pg >= 0 && pg < num_pages;
+  bad |= !ok;
+  return ok ? (int32_t)((int64_t)pg * kPage + (raw & (kPage - 1))) : -1;
 }
 
 // keep the larger (or smaller) of each register and its partner's
@@ -61,9 +70,8 @@ __device__ __forceinline__ void sort_in_thread(uint64_t (&v)[E], int g0, int siz
 // two emitted keys are equal (a position listed twice by the shard merge).
 template <int TOPK, bool SCORES = false, bool DUP = false>
 __device__ __forceinline__ void sort_emit(uint64_t* buf, int tid, const int32_t* row_pt,
-                                          int32_t* out_raw, int32_t* out_phys,
-                                          float* out_score = nullptr,
-                                          PlanHeader* dup_hdr = nullptr) {
+                                          int32_t num_pages, PlanHeader* hdr, int32_t* out_raw,
+                                          int32_t* out_phys, float* out_score = nullptr) {
   constexpr int E = TOPK / kFinThreads;
   static_assert(E == 2 || E == 4, "keys per thread");
   const int g0 = tid * E;
@@ -118,13 +126,14 @@ __device__ __forceinline__ void sort_emit(uint64_t* buf, int tid, const int32_t*
       const int i = g0 + e;
       dup |= i + 1 < TOPK && v[e] != 0ull && buf[i + 1] == v[e];
     }
-    if (dup) raise_status(dup_hdr, kErrInvalidMetadata, 422);
+    if (dup) raise_status(hdr, kErrInvalidMetadata, 422);
   }
   int32_t raw[E], phys[E];
+  bool bad_page = false;
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     raw[e] = v[e] != 0ull ? key_index(v[e]) : -1;
-    phys[e] = map_phys(row_pt, raw[e]);
+    phys[e] = map_phys(row_pt, raw[e], num_pages, bad_page);
     if (SCORES) out_score[g0 + e] = key_score(v[e]);
   }
   // E consecutive outputs per thread; rows start at multiples of 2 KB of a
@@ -137,6 +146,7 @@ __device__ __forceinline__ void sort_emit(uint64_t* buf, int tid, const int32_t*
     if (out_raw) *reinterpret_cast<int2*>(out_raw + g0) = make_int2(raw[0], raw[1]);
     if (out_phys) *reinterpret_cast<int2*>(out_phys + g0) = make_int2(phys[0], phys[1]);
   }
+  if (bad_page) raise_status(hdr, kErrInvalidPage, 440);
 }
 
 // A row whose block ran as a single work unit has at most TOPK candidates, all
@@ -245,12 +255,14 @@ __device__ __forceinline__ void team_rows(const FinishParams& p, int64_t blk, Te
   const int t = tw * 32 + lane;  // thread within the team
   // a context shard scores every nonempty clipped window, however short
   if (len <= (SCORES ? 0 : TOPK)) {
+    bool bad_page = false;
     for (int i = t; i < TOPK; i += 32 * W) {
       const int32_t raw = i < len ? s0 + i : -1;
       if (out_raw) out_raw[i] = raw;
-      if (out_phys) out_phys[i] = map_phys(row_pt, raw);
+      if (out_phys) out_phys[i] = map_phys(row_pt, raw, p.num_pages, bad_page);
       if (SCORES) out_score[i] = __uint_as_float(0x7FC00000u);
     }
+    if (bad_page) raise_status(p.hdr, kErrInvalidPage, 441);
     return;
   }
   const BlockInfo bi = p.blocks[p.row_block[r]];
@@ -272,13 +284,14 @@ __device__ __forceinline__ void team_rows(const FinishParams& p, int64_t blk, Te
   team_sort<TOPK>(v, g0, lane, xbuf + (W == 2 ? team * TOPK : 0), bar_id);
   // the lane now holds ranks g0 .. g0 + 15; rows start at multiples of 2 KB
   // of a 16-byte aligned base
+  bool bad_page = false;
 #pragma unroll
   for (int e = 0; e < kTeamE; e += 4) {
     int32_t raw[4], phys[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       raw[k] = v[e + k] != 0ull ? key_index(v[e + k]) : -1;
-      phys[k] = map_phys(row_pt, raw[k]);
+      phys[k] = map_phys(row_pt, raw[k], p.num_pages, bad_page);
     }
     if (out_raw)
       *reinterpret_cast<int4*>(out_raw + g0 + e) = make_int4(raw[0], raw[1], raw[2], raw[3]);
@@ -288,6 +301,7 @@ __device__ __forceinline__ void team_rows(const FinishParams& p, int64_t blk, Te
       *reinterpret_cast<float4*>(out_score + g0 + e) =
           make_float4(key_score(v[e]), key_score(v[e + 1]), key_score(v[e + 2]), key_score(v[e + 3]));
   }
+  if (bad_page) raise_status(p.hdr, kErrInvalidPage, 442);
 }
 
 // Shared memory of a finishing CTA.
@@ -327,11 +341,13 @@ __device__ __forceinline__ void finish_row(const FinishParams& p, int64_t r, Fin
 
   if (len <= (SCORES ? 0 : TOPK)) {
     if constexpr (DENSE) {
+      bool bad_page = false;
       for (int i = tid; i < TOPK; i += kFinThreads) {
         const int32_t raw = i < len ? s0 + i : -1;
         if (out_raw) out_raw[i] = raw;
-        if (out_phys) out_phys[i] = map_phys(row_pt, raw);
+        if (out_phys) out_phys[i] = map_phys(row_pt, raw, p.num_pages, bad_page);
       }
+      if (bad_page) raise_status(p.hdr, kErrInvalidPage, 443);
     }
     return;  // the merge's short rows are team_rows'
   }
@@ -491,7 +507,8 @@ __device__ __forceinline__ void finish_row(const FinishParams& p, int64_t r, Fin
     for (int i = n + tid; i < TOPK; i += kFinThreads) buf[i] = 0ull;
   }
   __syncthreads();
-  sort_emit<TOPK, SCORES, SRC == kSrcShards>(buf, tid, row_pt, out_raw, out_phys, out_score, p.hdr);
+  sort_emit<TOPK, SCORES, SRC == kSrcShards>(buf, tid, row_pt, p.num_pages, p.hdr, out_raw,
+                                            out_phys, out_score);
 }
 
 // Rows r = blk, blk + nblk, ...; the status is read once per row by one
@@ -643,11 +660,13 @@ __global__ void __launch_bounds__(kFinThreads) tile_merge_kernel(TileMergeParams
   const int32_t* row_pt = p.page_table + (int64_t)p.row_req[r] * p.max_pages;
   if (len <= TOPK) {
     if (!p.last) return;
+    bool bad_page = false;
     for (int i = tid; i < TOPK; i += kFinThreads) {
       const int32_t raw = i < len ? s0 + i : -1;
       if (p.out_raw) p.out_raw[(int64_t)r * TOPK + i] = raw;
-      p.out_phys[(int64_t)r * TOPK + i] = map_phys(row_pt, raw);
+      p.out_phys[(int64_t)r * TOPK + i] = map_phys(row_pt, raw, p.num_pages, bad_page);
     }
+    if (bad_page) raise_status(p.hdr, kErrInvalidPage, 444);
     return;
   }
   uint64_t* run = p.run_keys + (int64_t)r * TOPK;
@@ -692,8 +711,8 @@ __global__ void __launch_bounds__(kFinThreads) tile_merge_kernel(TileMergeParams
     for (int i = n + tid; i < TOPK; i += kFinThreads) buf[i] = 0ull;
   }
   __syncthreads();
-  sort_emit<TOPK>(buf, tid, row_pt, p.out_raw ? p.out_raw + (int64_t)r * TOPK : nullptr,
-                  p.out_phys + (int64_t)r * TOPK);
+  sort_emit<TOPK>(buf, tid, row_pt, p.num_pages, p.hdr,
+                  p.out_raw ? p.out_raw + (int64_t)r * TOPK : nullptr, p.out_phys + (int64_t)r * TOPK);
 }
 }  // namespace
 

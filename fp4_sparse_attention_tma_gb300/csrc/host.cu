@@ -35,7 +35,7 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
 // Optional per-kernel timing of the last call (CUDA events on the caller's
-// stream around each launch): plan+page check, scorer, finish, whole call.
+// stream around each launch): plan, scorer, finish, whole call.
 std::atomic<bool> g_timing{false};
 thread_local float g_last_ms[4] = {0.f, 0.f, 0.f, 0.f};
 
@@ -534,6 +534,7 @@ int run(const Call& c, cudaStream_t stream) {
     fp.page_table = pp.page_table;
     fp.rows = pp.rows;
     fp.max_pages = pp.max_pages;
+    fp.num_pages = pp.num_pages;
     fp.topk = c.topk;
     fp.hdr = pp.hdr;
     fp.row_block = pp.row_block;
@@ -716,6 +717,7 @@ int run_fixed_scratch(const Call& c, cudaStream_t stream) {
   fp.page_table = pp.page_table;
   fp.rows = pp.rows;
   fp.max_pages = pp.max_pages;
+  fp.num_pages = pp.num_pages;
   fp.topk = c.topk;
   fp.hdr = pp.hdr;
   fp.row_block = pp.row_block;
@@ -887,6 +889,7 @@ int run_tiled(const Call& c, int32_t tile, cudaStream_t stream) {
     mp.page_table = pp.page_table;
     mp.rows = (int32_t)R;
     mp.max_pages = pp.max_pages;
+    mp.num_pages = pp.num_pages;
     mp.topk = c.topk;
     mp.c0 = c0;
     mp.c1 = c1;
@@ -1043,6 +1046,7 @@ int run_shard(const Call& c, int32_t c0, int32_t c1, const idx_tensor_t* out_sco
   fp.page_table = nullptr;  // a shard emits positions and scores, no slots
   fp.rows = pp.rows;
   fp.max_pages = pp.max_pages;
+  fp.num_pages = pp.num_pages;
   fp.topk = c.topk;
   fp.hdr = pp.hdr;
   fp.row_block = pp.row_block;
@@ -1122,6 +1126,9 @@ int run_merge_shards(const idx_tensor_t* shard_score, const idx_tensor_t* shard_
   fp.page_table = (const int32_t*)page_table->data;
   fp.rows = (int32_t)R;
   fp.max_pages = (int32_t)max_pages;
+  // the K cache is not an argument of the merge: its page count is unknown here,
+  // so a mapped entry is only required to be non-negative
+  fp.num_pages = INT32_MAX;
   fp.topk = topk;
   fp.hdr = s.hdr();
   fp.n_shards = (int32_t)S;
@@ -1263,6 +1270,7 @@ int run_stream_ordered(const Call& c, void* workspace, uint64_t workspace_bytes,
   fp.page_table = pp.page_table;
   fp.rows = pp.rows;
   fp.max_pages = pp.max_pages;
+  fp.num_pages = pp.num_pages;
   fp.topk = c.topk;
   fp.hdr = pp.hdr;
   fp.row_block = pp.row_block;

@@ -174,7 +174,8 @@ struct TileMergeParams {
   const int32_t* row_start;   // the full windows
   const int32_t* row_end;
   const int32_t* page_table;
-  int32_t rows, max_pages, topk, c0, c1, first, last, pad;
+  int32_t rows, max_pages, topk, c0, c1, first, last;
+  int32_t num_pages;          // pages of the K cache: a mapped entry must lie in [0, num_pages)
   int64_t stride;             // floats per row of the chunk buffer
   const float* chunk;         // [rows, stride], column = slot - c0
   uint64_t* run_keys;         // [rows, topk] running candidates
@@ -192,7 +193,8 @@ struct FinishParams {
   const int32_t* row_start;
   const int32_t* row_end;
   const int32_t* page_table;  // null: no physical mapping
-  int32_t rows, max_pages, topk, pad;
+  int32_t rows, max_pages, topk;
+  int32_t num_pages;          // a mapped page-table entry must lie in [0, num_pages)
   PlanHeader* hdr;            // status word (and plan for the merge)
   const int32_t* row_block;
   const BlockInfo* blocks;

@@ -32,7 +32,7 @@ inline cudaError_t set_smem_once(Kernel kernel, int bytes, std::atomic<bool> (&d
 // kErrTimeout is recorded in hdr after the wait limit).
 cudaError_t launch_wait_probe(PlanHeader* hdr, bool never, cudaStream_t stream);
 
-// plan_kernel (1 CTA) then validate_pages_kernel.
+// plan_kernel (1 CTA): row validation, blocks, units and their schedule.
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 
 // Persistent scoring kernel, `grid` CTAs.  mode kModeSelect writes unit

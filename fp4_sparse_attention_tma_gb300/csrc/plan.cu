@@ -17,7 +17,7 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 constexpr int kRowsPerThread = 8;
-constexpr int kSortMax = 8192;  // units sorted by length when at most this many
+constexpr int kLenClasses = 64;  // length classes of the longest-first schedule order
 
 template <typename T, typename Op>
 __device__ T block_scan_incl(T v, T* warp_tot, Op op, T identity) {
@@ -56,7 +56,6 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   __shared__ int32_t s_tot32[32];
   __shared__ int64_t s_carry_blocks;
   __shared__ int32_t s_carry_seg;
-  extern __shared__ __align__(16) uint64_t s_sort[];
   const int tid = threadIdx.x;
   PlanHeader* hdr = p.hdr;
   if (p.clear_hdr) {
@@ -247,43 +246,44 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   if (read_status(hdr) != kOk) return;
 
   // 5. schedule: longest units first (the scorer deals them to its persistent
-  //    CTAs band by band, alternating the direction).  With no more units than
-  //    CTAs every unit starts at once and the order cannot matter.  Units of
-  //    nearly equal length (longest <= 1.25 x shortest) are not sorted: the
-  //    alternating deal balances them in any order, and they are dealt last
-  //    block first (a request's later rows have the longer causal windows, so
-  //    this is close to longest first and keeps the short ones for the last,
-  //    partial band).
+  //    CTAs band by band, alternating the direction, or its CTAs claim them in
+  //    this order).  With no more units than CTAs every unit starts at once and
+  //    the order cannot matter.  Units of nearly equal length (longest <= 1.25
+  //    x shortest) are not ordered: the alternating deal balances them in any
+  //    order, and they are dealt last block first (a request's later rows have
+  //    the longer causal windows, so this is close to longest first and keeps
+  //    the short ones for the last, partial band).  Otherwise the order is by
+  //    kLenClasses length classes of equal width, longest class first (a count
+  //    per class, a scan, then each unit to the next free position of its
+  //    class): within a class the lengths differ by less than 1/kLenClasses of
+  //    the longest unit, and their order is not fixed.
   const bool spread = 4ll * s_len_max > 5ll * s_len_min;
-  if (n_units > p.grid && n_units <= kSortMax && spread) {
-    int64_t n2 = 1;
-    while (n2 < n_units) n2 <<= 1;
-    for (int64_t i = tid; i < n2; i += kPlanThreads) {
-      uint64_t key = 0;
-      if (i < n_units) {
-        UnitInfo u = p.units[i];
-        key = ((uint64_t)(uint32_t)(u.t_end - u.t_begin) << 32) | (uint64_t)(~(uint32_t)i);
+  if (n_units > p.grid && spread) {
+    __shared__ uint32_t s_cls[kLenClasses];
+    const int32_t width = (s_len_max + kLenClasses) / kLenClasses;  // ceil((max + 1) / classes)
+    auto cls_of = [&](int64_t i) -> int {
+      const UnitInfo u = p.units[i];
+      return kLenClasses - 1 - (u.t_end - u.t_begin) / width;
+    };
+    for (int c = tid; c < kLenClasses; c += kPlanThreads) s_cls[c] = 0;
+    __syncthreads();
+    for (int64_t i = tid; i < n_units; i += kPlanThreads) atomicAdd(&s_cls[cls_of(i)], 1u);
+    __syncthreads();
+    if (tid < 32) {  // exclusive scan of the class counts, two per lane
+      static_assert(kLenClasses == 64, "two classes per lane");
+      const uint32_t a = s_cls[2 * tid], b = s_cls[2 * tid + 1];
+      uint32_t x = a + b;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (tid >= o) x += y;
       }
-      s_sort[i] = key;
+      s_cls[2 * tid] = x - (a + b);
+      s_cls[2 * tid + 1] = x - b;
     }
     __syncthreads();
-    for (int64_t size = 2; size <= n2; size <<= 1) {
-      for (int64_t stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int64_t i = tid; i < n2 / 2; i += kPlanThreads) {
-          int64_t lo = 2 * i - (i & (stride - 1));
-          int64_t hi = lo + stride;
-          uint64_t a = s_sort[lo], c = s_sort[hi];
-          bool desc = (lo & size) == 0;
-          if (desc ? (a < c) : (a > c)) {
-            s_sort[lo] = c;
-            s_sort[hi] = a;
-          }
-        }
-        __syncthreads();
-      }
-    }
     for (int64_t i = tid; i < n_units; i += kPlanThreads)
-      p.sched[i] = (int32_t)(~(uint32_t)(s_sort[i] & 0xffffffffu));
+      p.sched[atomicAdd(&s_cls[cls_of(i)], 1u)] = (int32_t)i;
   } else if (n_units > p.grid) {
     for (int64_t i = tid; i < n_units; i += kPlanThreads) p.sched[i] = (int32_t)(n_units - 1 - i);
   } else {
@@ -294,62 +294,6 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     hdr->n_units = (int32_t)n_units;
     hdr->unit_tiles = (int32_t)unit_tiles;
     hdr->n_row_slots = s_slot_carry;
-  }
-}
-
-// One warp per row block: every page-table entry that the window [start, end)
-// of a row the scorer does not score (end - start <= score_thr) touches must
-// name a page in [0, num_pages).  The finishing step maps such a row's
-// positions through the page table.  The entries under a scored row's window
-// are checked by the scorer's producer warps, which read each of them before
-// the page's copy and raise the same error for an entry outside the range.
-__global__ void __launch_bounds__(256) validate_pages_kernel(PlanParams p) {
-  PlanHeader* hdr = p.hdr;
-  if (read_status(hdr) != kOk) return;
-  const int lane = threadIdx.x & 31;
-  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int32_t n_blocks = hdr->n_blocks;
-  for (int64_t b = warp; b < n_blocks; b += nwarps) {
-    BlockInfo bi = p.blocks[b];
-    int32_t s[kRowsPerBlock], e[kRowsPerBlock];
-    int32_t lo = INT32_MAX, hi = 0;
-    for (int j = 0; j < kRowsPerBlock; ++j) {
-      s[j] = 0;
-      e[j] = 0;
-      if (j < bi.nrows) {
-        s[j] = p.row_start[bi.row0 + j];
-        e[j] = p.row_end[bi.row0 + j];
-        if (e[j] - s[j] > p.score_thr) e[j] = s[j];  // scored: the scorer checks its pages
-        if (e[j] > s[j]) {
-          lo = min(lo, s[j]);
-          hi = max(hi, e[j]);
-        }
-      }
-    }
-    if (hi <= lo) continue;
-    const int32_t p0 = lo / kPage, p1 = (hi + kPage - 1) / kPage;
-    const int32_t* row_pt = p.page_table + (int64_t)bi.req * p.max_pages;
-    bool bad = false;
-    // kPtUnroll independent entry loads per lane are in flight before any is
-    // checked (a long window has thousands of entries)
-    constexpr int kPtUnroll = 8;
-    for (int32_t base = p0; base < p1; base += 32 * kPtUnroll) {
-      int32_t v[kPtUnroll];
-      bool need[kPtUnroll];
-#pragma unroll
-      for (int u = 0; u < kPtUnroll; ++u) {
-        const int32_t pg = base + 32 * u + lane;
-        need[u] = false;
-        if (pg < p1)
-          for (int j = 0; j < kRowsPerBlock; ++j)
-            need[u] |= (s[j] < (pg + 1) * kPage) && (e[j] > pg * kPage) && (e[j] > s[j]);
-        v[u] = need[u] ? row_pt[pg] : 0;
-      }
-#pragma unroll
-      for (int u = 0; u < kPtUnroll; ++u) bad |= need[u] && ((v[u] < 0) || (v[u] >= p.num_pages));
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) raise_status(hdr, kErrInvalidPage, 120);
   }
 }
 
@@ -381,17 +325,9 @@ cudaError_t launch_wait_probe(PlanHeader* hdr, bool never, cudaStream_t stream) 
 }
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
-  static const size_t kSortBytes = sizeof(uint64_t) * kSortMax;
-  static std::atomic<bool> done[64] = {};
-  cudaError_t err = set_smem_once(plan_kernel, (int)kSortBytes, done);
-  if (err != cudaSuccess) return err;
-  plan_kernel<<<1, kPlanThreads, kSortBytes, stream>>>(p);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  int blocks = p.grid > 0 ? p.grid * 4 : 128;
-  const int need = (p.rows + 7) / 8;  // one warp per row block, at most one block per row
-  if (blocks > need) blocks = need > 0 ? need : 1;
-  validate_pages_kernel<<<blocks, 256, 0, stream>>>(p);
+  // (the page-table entries are checked where they are read: by the scorer's
+  // producers for the scored rows, by the finishing step's mapping for the rest)
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

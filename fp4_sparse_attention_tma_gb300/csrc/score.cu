@@ -105,6 +105,13 @@ constexpr uint32_t kIdescK1 = idesc_mxf4(128, kAccCols, 2);
 // its four regions and each warp compacts its own region in place.  A region never has to hold more than topk survivors plus
 // one check window of appends.
 constexpr int kCheckTiles = 12;
+// At topk 512 a unit of at most kShortUnitTiles tiles compacts as soon as a
+// region holds more than kShortTrig keys (at the first vote when the row's
+// window covers the first 12 tiles: 4 x 384 keys for 512), so that its
+// threshold rises early and its later tiles append few keys.  Longer units and
+// topk 1024 keep the late trigger (an early one measured slower there).
+constexpr int kShortUnitTiles = 96;
+constexpr uint32_t kShortTrig = 383;
 constexpr uint32_t kBarVote = 4;  // named barrier of the compaction vote (1..3: row groups)
 // The candidate buffers take all shared memory the pipeline leaves free.
 constexpr uint32_t kMaxSmem = 227u * 1024u;
@@ -502,7 +509,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           int c = 0;
           if (lane == 0) {
-            c = (int)atomicAdd(&hdr->claim, 1u);
+            // the first unit of CTA b is schedule position b (no round trip to
+            // the counter when the call starts); the later ones are claimed
+            // from position gridDim.x on
+            c = i == 0 ? (int)blockIdx.x : (int)gridDim.x + (int)atomicAdd(&hdr->claim, 1u);
             if (c >= n_units) c = -1;
             unit_slot[qb] = c;
           }
@@ -650,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool v0 = need0 && pg0 >= 0 && pg0 < p.num_pages;
           const bool v1 = need1 && pg1 >= 0 && pg1 < p.num_pages;
           // this is the page-table check of the scored rows' windows (the
-          // planner's page check covers only the rows that are not scored)
+          // finishing step checks the entries it maps for the other rows)
           if ((need0 && !v0) || (need1 && !v1)) raise_status(hdr, kErrInvalidPage, 303);
           const uint32_t bytes = ((uint32_t)v0 + (uint32_t)v1) * kPageBytes;
           if (bytes) {
@@ -846,6 +856,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16) + kColAcc + 64u * g;
           int check_in = kCheckTiles;  // tiles until the next over-limit check
+          const uint32_t trig = (TOPK == 512 && uv.u.t_end - uv.u.t_begin <= kShortUnitTiles)
+                                    ? kShortTrig
+                                    : warp_region(TOPK) - kCheckTiles * 32u;
           // scored rows of the block: their warps take part in the votes (every
           // epilogue warp computes the same count from the same row windows)
           uint32_t n_act = 0;
@@ -924,7 +937,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               // load is in flight here)
               if (--check_in == 0) {
                 check_in = kCheckTiles;
-                const bool over = wcnt > warp_region(TOPK) - kCheckTiles * 32u;
+                const bool over = wcnt > trig;
                 if (lane == 0) wc_s[qd] = wcnt;  // visible to the group after the vote
                 // one vote for the whole block: when any row needs it, every
                 // scored row compacts at the same tile, so that their pauses

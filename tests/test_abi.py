@@ -136,3 +136,26 @@ def test_every_declaration_cites_its_passage():
         j = before.rfind("/*")
         comment = re.sub(r"\s*\n\s*\*\s?", " ", before[j:before.rfind("*/")])
         assert re.search(r"aiter#\d+|sglang#\d+|no counterpart on the pages", comment), m.group(1)
+
+
+def test_packed_descriptors_match_the_struct_layout():
+    """The binding packs idx_tensor_t descriptors into one buffer per call: the
+    bytes must be those of the ctypes struct (data, dtype, ndim, shape[4],
+    stride[4]) for every tensor shape the entry points take."""
+    import ctypes
+    import torch
+    import fp4_sparse_attention_tma_gb300 as m
+    ts = [torch.zeros((7, 64, 64), dtype=torch.uint8), torch.zeros(5, dtype=torch.int32),
+          torch.zeros((3, 4), dtype=torch.float32)[:, ::2], torch.zeros(0, dtype=torch.int32),
+          torch.zeros((2, 3, 4, 5), dtype=torch.float32), torch.zeros((2, 3, 4, 5, 6)),
+          torch.zeros((6, 2), dtype=torch.float64), None]
+    buf, addrs = m._descs(ts)
+    assert ctypes.sizeof(_lib.IdxTensor) == m._DESC.size == 80
+    for i, t in enumerate(ts):
+        if t is None:
+            assert addrs[i] is None
+            continue
+        assert addrs[i] == ctypes.addressof(buf) + 80 * i
+        want = bytes(m._desc(t))
+        got = ctypes.string_at(addrs[i], 80)
+        assert got == want, (i, tuple(t.shape))

@@ -123,8 +123,9 @@ def test_overflow_descriptor_rejected(base):
     phys = torch.zeros((base.rows, 512), dtype=torch.int32, device="cuda")
     order = ["q_fp4", "q_scale", "k_cache_fp4", "k_scale", "weights", "page_table", "row_req",
              "row_start", "row_end"]
-    code = lib.idx_topk_fp4_prefill(*[ctypes.byref(descs[k]) for k in order], 512,
-                                    ctypes.byref(m._desc(phys)), None,
+    phys_d = m._desc(phys)
+    code = lib.idx_topk_fp4_prefill(*[ctypes.addressof(descs[k]) for k in order], 512,
+                                    ctypes.addressof(phys_d), None,
                                     ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     torch.cuda.synchronize()
     assert code == 5
