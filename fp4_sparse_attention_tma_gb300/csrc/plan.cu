@@ -15,8 +15,13 @@ namespace idxk {
 
 namespace {
 
-constexpr int kPlanThreads = 1024;
 constexpr int kRowsPerThread = 8;
+constexpr int kPlanThreads = 1024;      // calls of more than kPlanSmallRows rows
+// decode-sized calls: 4 warps (their block-wide scans and barriers are cheaper;
+// at 1024 rows the extra tiles of the block loops cost more than that saves)
+constexpr int kPlanThreadsSmall = 128;
+constexpr int kPlanSmallRows = 256;
+static_assert(kPlanSmallRows <= kPlanThreadsSmall * kRowsPerThread, "one tile of rows");
 constexpr int kLenClasses = 64;  // length classes of the longest-first schedule order
 
 template <typename T, typename Op>
@@ -51,7 +56,8 @@ struct MaxI32 {
   __device__ int32_t operator()(int32_t a, int32_t b) const { return a > b ? a : b; }
 };
 
-__global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
+template <int NT>
+__global__ void __launch_bounds__(NT, 1) plan_kernel(PlanParams p) {
   __shared__ int64_t s_tot64[32];
   __shared__ int32_t s_tot32[32];
   __shared__ int64_t s_carry_blocks;
@@ -66,7 +72,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   }
 
   // 1. row metadata
-  for (int r = tid; r < p.rows; r += kPlanThreads) {
+  for (int r = tid; r < p.rows; r += NT) {
     int32_t req = p.row_req[r], s = p.row_start[r], e = p.row_end[r];
     bool ok = req >= 0 && req < p.num_req && s >= 0 && e >= s &&
               (int64_t)e <= (int64_t)p.max_pages * kPage && (p.check_end_le < 0 || e <= p.check_end_le);
@@ -82,7 +88,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     s_carry_seg = 0;
   }
   __syncthreads();
-  for (int64_t base = 0; base < p.rows; base += (int64_t)kPlanThreads * kRowsPerThread) {
+  for (int64_t base = 0; base < p.rows; base += (int64_t)NT * kRowsPerThread) {
     const int64_t r0 = base + (int64_t)tid * kRowsPerThread;
     // the thread's rows' requests, loaded once: rq[k + 1] is row r0 + k's, rq[0]
     // the previous row's (-1 before row 0 and past the last row)
@@ -126,9 +132,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       p.row_block[r] = (int32_t)(b - 1);
     }
     __syncthreads();
-    if (tid == kPlanThreads - 1) {
+    if (tid == NT - 1) {
       s_carry_blocks += bincl;
-      int64_t last = base + (int64_t)kPlanThreads * kRowsPerThread - 1;
+      int64_t last = base + (int64_t)NT * kRowsPerThread - 1;
       if (last >= p.rows) last = p.rows - 1;
       // segment start of the last row of this tile
       int32_t sg = incl >= 0 ? incl : s_carry_seg;
@@ -142,7 +148,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
 
   // 3. per-block extent and tiles over the scored rows
   int64_t my_tiles = 0;
-  for (int64_t b = tid; b < n_blocks; b += kPlanThreads) {
+  for (int64_t b = tid; b < n_blocks; b += NT) {
     BlockInfo bi = p.blocks[b];
     int32_t next = (b + 1 < n_blocks) ? p.blocks[b + 1].row0 : p.rows;
     bi.nrows = next - bi.row0;
@@ -165,7 +171,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     p.blocks[b] = bi;
   }
   int64_t tot_tiles = block_scan_incl<int64_t>(my_tiles, s_tot64, AddI64(), 0);
-  if (tid == kPlanThreads - 1) s_tot64[0] = tot_tiles;
+  if (tid == NT - 1) s_tot64[0] = tot_tiles;
   __syncthreads();
   tot_tiles = s_tot64[0];
   __syncthreads();
@@ -176,7 +182,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   const int32_t ut = unit_tiles > INT32_MAX ? INT32_MAX : (int32_t)unit_tiles;
 
   // 4. units per block and candidate row-slots (blocks handled in tiles of
-  //    kPlanThreads with a running carry)
+  //    NT with a running carry)
   __shared__ int64_t s_unit_carry, s_slot_carry;
   __shared__ int32_t s_len_min, s_len_max;  // unit lengths in tiles
   if (tid == 0) {
@@ -186,7 +192,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     s_len_max = 0;
   }
   __syncthreads();
-  for (int64_t base = 0; base < n_blocks; base += kPlanThreads) {
+  for (int64_t base = 0; base < n_blocks; base += NT) {
     int64_t b = base + tid;
     int64_t nu = 0, ns = 0;
     BlockInfo bi{};
@@ -236,7 +242,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       }
     }
     __syncthreads();
-    if (tid == kPlanThreads - 1) {
+    if (tid == NT - 1) {
       s_unit_carry += u_incl;
       s_slot_carry += s_incl;
     }
@@ -265,9 +271,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       const UnitInfo u = p.units[i];
       return kLenClasses - 1 - (u.t_end - u.t_begin) / width;
     };
-    for (int c = tid; c < kLenClasses; c += kPlanThreads) s_cls[c] = 0;
+    for (int c = tid; c < kLenClasses; c += NT) s_cls[c] = 0;
     __syncthreads();
-    for (int64_t i = tid; i < n_units; i += kPlanThreads) atomicAdd(&s_cls[cls_of(i)], 1u);
+    for (int64_t i = tid; i < n_units; i += NT) atomicAdd(&s_cls[cls_of(i)], 1u);
     __syncthreads();
     if (tid < 32) {  // exclusive scan of the class counts, two per lane
       static_assert(kLenClasses == 64, "two classes per lane");
@@ -282,12 +288,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       s_cls[2 * tid + 1] = x - b;
     }
     __syncthreads();
-    for (int64_t i = tid; i < n_units; i += kPlanThreads)
+    for (int64_t i = tid; i < n_units; i += NT)
       p.sched[atomicAdd(&s_cls[cls_of(i)], 1u)] = (int32_t)i;
   } else if (n_units > p.grid) {
-    for (int64_t i = tid; i < n_units; i += kPlanThreads) p.sched[i] = (int32_t)(n_units - 1 - i);
+    for (int64_t i = tid; i < n_units; i += NT) p.sched[i] = (int32_t)(n_units - 1 - i);
   } else {
-    for (int64_t i = tid; i < n_units; i += kPlanThreads) p.sched[i] = (int32_t)i;
+    for (int64_t i = tid; i < n_units; i += NT) p.sched[i] = (int32_t)i;
   }
   if (tid == 0) {
     hdr->n_blocks = (int32_t)n_blocks;
@@ -327,7 +333,10 @@ cudaError_t launch_wait_probe(PlanHeader* hdr, bool never, cudaStream_t stream) 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
   // (the page-table entries are checked where they are read: by the scorer's
   // producers for the scored rows, by the finishing step's mapping for the rest)
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
+  if (p.rows <= kPlanSmallRows)
+    plan_kernel<kPlanThreadsSmall><<<1, kPlanThreadsSmall, 0, stream>>>(p);
+  else
+    plan_kernel<kPlanThreads><<<1, kPlanThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
