@@ -53,6 +53,75 @@ def test_invalid_page_entry(base):
     assert _call(base, d)[0] == 4
 
 
+@pytest.fixture(scope="module")
+def short_rows():
+    # request 0 has only rows of at most topk positions (not scored: every
+    # position is emitted and mapped through the page table); request 1 a
+    # scored row
+    return inputs.make_problem(53, [700, 3000], [[(0, 300), (100, 612)], [(0, 3000)]], topk=512)
+
+
+@pytest.mark.parametrize("page,expect", [(0, 4), (2, 4), (9, 4), (10, 0), (20, 0)])
+def test_page_check_covers_unscored_rows(short_rows, page, expect):
+    """An entry under a row that is not scored is checked where the finishing
+    step maps the row's positions: pages 0..9 lie under request 0's windows
+    [0, 300) and [100, 612); page 10 and later do not and are never read."""
+    p = short_rows
+    for bad in (-1, p.num_pages):
+        d = H.to_device(p)
+        d["page_table"][0, page] = bad
+        code, phys, raw = _call(p, d)
+        assert code == expect
+        if expect:
+            assert np.all(phys == -1) and np.all(raw == -1)
+
+
+def test_page_check_unscored_rows_stream_ordered(short_rows):
+    """The stream-ordered call publishes the same status from the finishing
+    kernel's last CTA, with -1 outputs."""
+    import torch
+    import fp4_sparse_attention_tma_gb300 as m
+    p = short_rows
+    d = H.to_device(p)
+    d["page_table"][0, 4] = p.num_pages + 3
+    ws = torch.empty(m.idx_topk_fp4_scratch_bytes(p.rows, 512), dtype=torch.uint8, device="cuda")
+    st = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+    phys = torch.full((p.rows, 512), 7, dtype=torch.int32, device="cuda")
+    raw = torch.full((p.rows, 512), 7, dtype=torch.int32, device="cuda")
+    assert m.idx_topk_fp4_prefill_async(**d, topk=512, out_phys_slot=phys, out_raw_idx=raw,
+                                        workspace=ws, status=st, raise_on_error=False) == 0
+    torch.cuda.synchronize()
+    assert int(st.item()) == 4
+    assert (phys.cpu().numpy() == -1).all() and (raw.cpu().numpy() == -1).all()
+    d = H.to_device(p)
+    assert m.idx_topk_fp4_prefill_async(**d, topk=512, out_phys_slot=phys, out_raw_idx=raw,
+                                        workspace=ws, status=st, raise_on_error=False) == 0
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    code, want_phys, want_raw = _call(p, d)
+    assert code == 0
+    np.testing.assert_array_equal(phys.cpu().numpy(), want_phys)
+    np.testing.assert_array_equal(raw.cpu().numpy(), want_raw)
+
+
+def test_page_check_tiled_path(short_rows):
+    """The context-tiled path checks the entries it maps as well: under the
+    unscored rows (its last chunk's closed form) and under the scored row."""
+    import torch
+    import fp4_sparse_attention_tma_gb300 as m
+    p = short_rows
+    for req, page in ((0, 3), (1, 30)):
+        d = H.to_device(p)
+        d["page_table"][req, page] = -2
+        phys = torch.zeros((p.rows, 512), dtype=torch.int32, device="cuda")
+        raw = torch.zeros((p.rows, 512), dtype=torch.int32, device="cuda")
+        code = m.idx_tiled_topk_fp4_prefill(**d, topk=512, out_phys_slot=phys, out_raw_idx=raw,
+                                            context_tile=1024, raise_on_error=False)
+        torch.cuda.synchronize()
+        assert code == 4, (req, page)
+        assert (phys.cpu().numpy() == -1).all()
+
+
 def test_page_entries_outside_windows_are_not_read(base):
     d = H.to_device(base)
     # request 1's windows end at 900 -> logical pages >= 15 are never covered
