@@ -326,8 +326,8 @@ int idx_topk_scratch_high_water(int32_t device, uint64_t* bytes);
 
 /* Measurement support (no counterpart on the pages): when enabled, each call
  * of the calling thread records CUDA events on its stream around the kernel
- * phases; idx_topk_last_timings then returns, in milliseconds, {planning and
- * page validation, scoring kernel, finishing kernel, whole kernel sequence} of
+ * phases; idx_topk_last_timings then returns, in milliseconds, {planning,
+ * scoring kernel, finishing kernel, whole kernel sequence} of
  * that thread's last completed call.  Process-wide switch; default off. */
 int idx_topk_set_timing(int32_t enable);
 int idx_topk_last_timings(float* ms4);
