@@ -62,6 +62,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the per-workload lines and the fresh-process repeats")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="only the decode-shaped batches (graph replay and synchronous call)")
     ap.add_argument("--child-pairs", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -349,6 +351,77 @@ def other_workloads(m, local, flush, cfgs=(0, 1, 2, 4), steps=10, warm=3):
     return out
 
 
+def decode_latency(m, flush, reps=30):
+    """Decode-shaped batches (32 requests x 2 rows, contexts 4K-64K, topk 512
+    and 1024): the stream-ordered call captured into a CUDA graph and replayed
+    (median over `reps` replays, CUDA events around each; with the L2 flushed
+    before each replay, and back to back), and the synchronous call (L2
+    flushed before each).  The replay's outputs must equal the synchronous
+    call's and its device status must be 0."""
+    import numpy as np
+    import torch
+    from fp4_sparse_attention_tma_gb300 import inputs
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    out = []
+    for K in (512, 1024):
+        p = inputs.decode_batch(32, K)
+        dev = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).cuda()
+               for k in ("q_fp4", "q_scale", "k_cache_fp4", "k_scale", "weights", "page_table",
+                         "row_req", "row_start", "row_end")}
+        ws = torch.empty(m.idx_topk_fp4_scratch_bytes(p.rows, K), dtype=torch.uint8,
+                         device="cuda")
+        st = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+        phys = torch.empty((p.rows, K), dtype=torch.int32, device="cuda")
+        raw = torch.empty_like(phys)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                m.idx_topk_fp4_prefill_async(**dev, topk=K, out_phys_slot=phys, workspace=ws,
+                                             status=st, out_raw_idx=raw)
+        torch.cuda.current_stream().wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            m.idx_topk_fp4_prefill_async(**dev, topk=K, out_phys_slot=phys, workspace=ws,
+                                         status=st, out_raw_idx=raw)
+        cold, warm, sync = [], [], []
+        for i in range(reps + 3):
+            flush.zero_()
+            ev0.record()
+            g.replay()
+            ev1.record()
+            ev1.synchronize()
+            if i >= 3:
+                cold.append(ev0.elapsed_time(ev1) * 1e3)
+        for i in range(reps + 3):
+            ev0.record()
+            g.replay()
+            ev1.record()
+            ev1.synchronize()
+            if i >= 3:
+                warm.append(ev0.elapsed_time(ev1) * 1e3)
+        status = int(st.item())
+        g_phys, g_raw = phys.clone(), raw.clone()
+        s_phys, s_raw = torch.empty_like(phys), torch.empty_like(raw)
+        for i in range(13):
+            flush.zero_()
+            ev0.record()
+            m.idx_topk_fp4_prefill(**dev, topk=K, out_phys_slot=s_phys, out_raw_idx=s_raw)
+            ev1.record()
+            ev1.synchronize()
+            if i >= 3:
+                sync.append(ev0.elapsed_time(ev1) * 1e3)
+        out.append({"workload": p.name, "rows": p.rows, "topk": K,
+                    "graph_replay_us": statistics.median(cold),
+                    "graph_replay_warm_l2_us": statistics.median(warm),
+                    "sync_call_us": statistics.median(sync), "status": status,
+                    "indices_identical": bool(torch.equal(g_phys, s_phys) and
+                                              torch.equal(g_raw, s_raw))})
+        del g, dev, ws, phys, raw
+    return out
+
+
 def run_reference(args):
     """Reference arm: the CPU oracle on the host cores, same metric and workload."""
     import numpy as np
@@ -426,6 +499,12 @@ def main():
     phys = torch.empty((R, K), dtype=torch.int32, device="cuda")
     raw = torch.empty((R, K), dtype=torch.int32, device="cuda")
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    if args.decode_only:
+        if rank == 0:
+            print(json.dumps({"decode": decode_latency(m, flush)}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     def fused():
         m.idx_topk_fp4_prefill(**dev, topk=K, out_phys_slot=phys, out_raw_idx=raw)
@@ -557,6 +636,7 @@ def main():
 
     if rank == 0 and world == 1 and not args.no_extra:
         line["workloads"] = other_workloads(m, local, flush)
+        line["decode"] = decode_latency(m, flush)
         if not args.no_dense:
             line["fresh_processes"] = fresh_processes(args)
     if rank == 0 and world == 1 and not args.no_cpu:

@@ -221,6 +221,19 @@ def config(idx: int) -> Problem:
     raise ValueError(f"no workload {idx}")
 
 
+def decode_batch(n_req: int = 32, topk: int = 512, lo: int = 4096, hi: int = 65536,
+                 seed: int = 5) -> Problem:
+    """A decode-shaped batch: n_req requests whose C4 lengths L are drawn
+    uniformly from [lo, hi), two query rows each (a decode step with one
+    speculative token: windows [0, L - 1) and [0, L))."""
+    rng = np.random.default_rng(seed)
+    lens = [int(x) for x in rng.integers(lo, hi, size=n_req)]
+    return make_problem(seed, lens, [[(0, L - 1), (0, L)] for L in lens], topk,
+                        name=f"decode-{n_req}x2-K{topk}",
+                        recipe=f"{n_req} requests x 2 rows, C4 uniform in [{lo}, {hi}), "
+                               f"windows [0, L-1) and [0, L)")
+
+
 def k_scale_mma_order(k_scale: np.ndarray) -> np.ndarray:
     """A [NP, 64, 4] K-scale array rearranged (a pure permutation of bytes) into
     the [NP, 256] order of idx_topk_fp4_prefill_mma_scales: byte 8j + 4h + b of

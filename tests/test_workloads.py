@@ -110,3 +110,18 @@ def test_k_scale_mma_order_is_the_documented_permutation():
                 for b in range(4):
                     assert o[p, 8 * j + 4 * h + b] == k[p, 32 * h + j, b]
         assert sorted(o[p].tolist()) == sorted(k[p].ravel().tolist())
+
+
+def test_decode_batch_recipe():
+    """The bench's decode batch: 32 requests, two rows each with windows
+    [0, L-1) and [0, L), C4 lengths in [4096, 65536), deterministic."""
+    a = inputs.decode_batch(32, 512)
+    b = inputs.decode_batch(32, 512)
+    assert a.rows == 64 and a.topk == 512
+    np.testing.assert_array_equal(a.row_req, np.repeat(np.arange(32), 2))
+    L = a.row_end[1::2]
+    assert np.all(a.row_start == 0) and np.all(a.row_end[0::2] == L - 1)
+    assert np.all((L >= 4096) & (L < 65536))
+    np.testing.assert_array_equal(a.q_fp4, b.q_fp4)
+    np.testing.assert_array_equal(a.page_table, b.page_table)
+    assert inputs.decode_batch(32, 1024).topk == 1024
