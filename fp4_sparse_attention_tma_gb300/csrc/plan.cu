@@ -64,22 +64,31 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanParams p) {
   __shared__ int32_t s_carry_seg;
   const int tid = threadIdx.x;
   PlanHeader* hdr = p.hdr;
+  // small calls keep the block table in shared memory as well (phases 3 and
+  // 4 read it there instead of from global memory)
+  constexpr bool kCache = NT == kPlanThreadsSmall;
+  __shared__ BlockInfo s_blk[kCache ? kPlanSmallRows : 1];
   if (p.clear_hdr) {
     // the call's first kernel starts from an empty header (status kOk, no
     // claims); saves a separate clear on the stream
     if (tid == 0) *hdr = PlanHeader{};
     __syncthreads();
+  } else if (read_status(hdr) != kOk) {
+    return;  // an earlier kernel of the call failed (the same value in every thread)
   }
 
-  // 1. row metadata
+  // 1. row metadata (the CTA's own verdict decides, not a read of the status)
+  bool bad = false;
   for (int r = tid; r < p.rows; r += NT) {
     int32_t req = p.row_req[r], s = p.row_start[r], e = p.row_end[r];
     bool ok = req >= 0 && req < p.num_req && s >= 0 && e >= s &&
               (int64_t)e <= (int64_t)p.max_pages * kPage && (p.check_end_le < 0 || e <= p.check_end_le);
-    if (!ok) raise_status(hdr, kErrInvalidMetadata, 100);
+    if (!ok) {
+      raise_status(hdr, kErrInvalidMetadata, 100);
+      bad = true;
+    }
   }
-  __syncthreads();
-  if (read_status(hdr) != kOk) return;
+  if (__syncthreads_or(bad)) return;
 
   // 2. row blocks: a block starts at a request change or every kRowsPerBlock
   //    rows into a run of one request.
@@ -127,6 +136,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanParams p) {
         bi.row0 = (int32_t)r;
         bi.req = rq[k + 1];
         p.blocks[b] = bi;
+        if (kCache) s_blk[b] = bi;
         ++b;
       }
       p.row_block[r] = (int32_t)(b - 1);
@@ -149,8 +159,8 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanParams p) {
   // 3. per-block extent and tiles over the scored rows
   int64_t my_tiles = 0;
   for (int64_t b = tid; b < n_blocks; b += NT) {
-    BlockInfo bi = p.blocks[b];
-    int32_t next = (b + 1 < n_blocks) ? p.blocks[b + 1].row0 : p.rows;
+    BlockInfo bi = kCache ? s_blk[b] : p.blocks[b];
+    int32_t next = (b + 1 < n_blocks) ? (kCache ? s_blk[b + 1].row0 : p.blocks[b + 1].row0) : p.rows;
     bi.nrows = next - bi.row0;
     int32_t lo = INT32_MAX, hi = 0;
     for (int j = 0; j < bi.nrows; ++j) {
@@ -169,6 +179,11 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanParams p) {
     }
     my_tiles += bi.ntiles;
     p.blocks[b] = bi;
+    if (kCache) {  // the fields this phase computes (row0, read by the neighbour, stays)
+      s_blk[b].nrows = bi.nrows;
+      s_blk[b].tile0 = bi.tile0;
+      s_blk[b].ntiles = bi.ntiles;
+    }
   }
   int64_t tot_tiles = block_scan_incl<int64_t>(my_tiles, s_tot64, AddI64(), 0);
   if (tid == NT - 1) s_tot64[0] = tot_tiles;
@@ -197,7 +212,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanParams p) {
     int64_t nu = 0, ns = 0;
     BlockInfo bi{};
     if (b < n_blocks) {
-      bi = p.blocks[b];
+      bi = kCache ? s_blk[b] : p.blocks[b];
       nu = bi.ntiles > 0 ? bi.ntiles / ut + (bi.ntiles % ut != 0) : 0;
       ns = nu * bi.nrows;
     }
@@ -208,6 +223,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanParams p) {
     if (b < n_blocks) {
       if (u_first + nu > p.max_units || s_first + ns > p.max_row_slots) {
         raise_status(hdr, kErrInternal, 110);
+        bad = true;
       } else {
         bi.n_units = (int32_t)nu;
         bi.unit_first = (int32_t)u_first;
@@ -249,7 +265,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanParams p) {
     __syncthreads();
   }
   const int64_t n_units = s_unit_carry;
-  if (read_status(hdr) != kOk) return;
+  if (__syncthreads_or(bad)) return;
 
   // 5. schedule: longest units first (the scorer deals them to its persistent
   //    CTAs band by band, alternating the direction, or its CTAs claim them in
