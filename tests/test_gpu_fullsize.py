@@ -82,10 +82,11 @@ def test_full_size_workload(cfg):
     check_workload(inputs.config(cfg))
 
 
-def test_more_units_than_the_planner_sorts():
+def test_many_units_of_spread_lengths():
     # 28,000 rows in 4 requests of 8,192 C4 positions: 9,336 row blocks, each one
-    # work unit of its own length (5 to 64 tiles) -- more units than the planner
-    # sorts, so they are dealt unsorted; random windows, some of them short
+    # work unit of its own length (5 to 64 tiles), far more units than CTAs, so
+    # the planner orders them by length class and the CTAs claim them; random
+    # windows, some of them short
     rng = np.random.default_rng(77)
     wins = []
     for _ in range(4):
