@@ -376,6 +376,9 @@ int idx_topk_fp4_prefill_shard(const idx_tensor_t* q_fp4, const idx_tensor_t* q_
  * outside its row's window, a position listed twice among the emitted TopK, or
  * a row whose lists hold fewer than topk positions although its window is
  * longer than topk returns IDX_ERR_INVALID_METADATA (as do bad row metadata);
+ * a negative page-table entry read by the mapping returns IDX_ERR_INVALID_PAGE
+ * (the K cache is not an argument, so entries are not compared with its page
+ * count here: the shard calls checked every entry under their windows);
  * unsupported topk IDX_ERR_UNSUPPORTED; outputs -1 on every error.  Scratch:
  * one status word.
  */
