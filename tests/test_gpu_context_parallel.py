@@ -148,3 +148,24 @@ def test_merge_fails_closed_on_malformed_lists():
     # a bad context range of a shard call
     code, sc, raw = _shard(p, d, 100, 50, raise_on_error=False)
     assert code == INVALID_ARGUMENT and bool((raw == -1).all()) and bool(torch.isnan(sc).all())
+
+
+def test_merge_fails_closed_on_negative_page_entry():
+    """The merge maps every emitted position through the page table; a negative
+    entry under an emitted position returns IDX_ERR_INVALID_PAGE with -1 outputs
+    (the short rows' positions are all emitted, so an entry under a short row's
+    window is always read)."""
+    p = inputs.small_problem(seed=45, topk=512)
+    d = H.to_device(p)
+    scores, raws = _sharded(p, d, _bounds(p, 2))
+    code, phys, raw = _merge(p, d, scores, raws)
+    assert code == 0
+    # a page under a position that the merge emits for row 0
+    r0 = 0
+    pos = int(raw[r0][raw[r0] >= 0][0])
+    req = int(p.row_req[r0])
+    bad = d["page_table"].clone()
+    bad[req, pos // 64] = -1
+    d2 = dict(d, page_table=bad)
+    code, phys, raw = _merge(p, d2, scores, raws, raise_on_error=False)
+    assert code == 4 and (phys == -1).all() and (raw == -1).all()
